@@ -1,0 +1,242 @@
+"""Seeded synthetic CSA2 decode workloads.
+
+This module only draws random tensors with the shapes and value
+distributions of the workloads; it contains none of the method's
+arithmetic (no scoring, selection, block summaries or attention).  Both the
+CPU oracle and the CUDA path consume what it produces, so neither side ever
+derives an input from the other.
+
+bf16 tensors are returned as their raw 16-bit patterns (numpy ``uint16``),
+obtained from float32 draws by round-to-nearest-even; fp32 tensors (the toy
+workload) are returned as ``float32``.
+
+Workloads (sizes from the DeepSeek-V4.1-Flash architecture page,
+"CSA2 with cross-layer reuse" and its bullet list: Top-512 main-KV entries
+plus a 128-token SWA window, blocks of 8, a pool of at most 2,048 blocks):
+
+* ``toy16`` -- the page's 16-token illustration ("How Full, Reuse and
+  Reindex pick tokens"): query at position 15, one compressed entry per
+  token, Top-3, SWA window 4, blocks of 2, a 4-block pool, Full mode.
+  4 query heads of dim 16, one shared KV head, 2 indexer heads of dim 8,
+  fp32 N(0,1) values.
+* ``full_b8_8k`` -- one Full layer, batch 8, 8,192 tokens at ratio 4
+  (2,048 entries), flat indexer.
+* ``enc_b32_32k`` -- encoder group Full + 5 Reuse, batch 32, 32,768 tokens at
+  ratio 4 (8,192 entries).
+* ``reindex_b64_128k`` -- one hierarchical Reindex layer, batch 64,
+  131,072 tokens at ratio 4 (32,768 entries = 4,096 blocks of 8), pool of
+  2,048 blocks.
+* ``dec_b16_1m`` -- decoder group Full + 3 Reuse + [Reindex + 3 Reuse] x 4,
+  batch 16, 1,048,576 tokens at ratio 4 (262,144 entries).
+
+Value recipe: main and SWA keys N(0,1)/sqrt(k_dim), values
+N(0,1)/sqrt(v_dim), queries N(0,1), all rounded to bf16; indexer queries
+and keys are bf16 integers uniform on {-4..4}; indexer head weights are
+fp32 integers uniform on {1,2,3}.
+"""
+from __future__ import annotations
+
+import dataclasses
+from typing import List, Optional
+
+import numpy as np
+
+FULL, REINDEX, REUSE = 0, 1, 2
+MODE_NAMES = {FULL: "full", REINDEX: "reindex", REUSE: "reuse"}
+
+
+def f32_to_bf16_bits(x: np.ndarray) -> np.ndarray:
+    """Round float32 values to bf16 (nearest, ties to even); return bit patterns."""
+    u = np.ascontiguousarray(x, dtype=np.float32).view(np.uint32)
+    u = u + (((u >> np.uint32(16)) & np.uint32(1)) + np.uint32(0x7FFF))
+    return (u >> np.uint32(16)).astype(np.uint16)
+
+
+@dataclasses.dataclass
+class Shape:
+    batch: int
+    n_entries: int        # capacity of the main-KV / indexer-key caches per sequence
+    idx_heads: int = 8
+    idx_dim: int = 64
+    block: int = 8
+    pool_blocks: int = 2048
+    topk: int = 512
+    q_heads: int = 64
+    k_dim: int = 192
+    v_dim: int = 128
+    swa: int = 128
+    scale: float = 0.0    # 0 -> 1/sqrt(k_dim)
+    relu: int = 1
+    dtype: str = "bf16"   # "bf16" or "f32"
+
+    @property
+    def softmax_scale(self) -> float:
+        return self.scale if self.scale > 0 else 1.0 / float(np.sqrt(self.k_dim))
+
+
+@dataclasses.dataclass
+class Layer:
+    mode: int
+    hier: int                        # 1: hierarchical block pool before token scoring
+    q: np.ndarray                    # [B, H, k_dim]
+    k_swa: np.ndarray                # [B, W, k_dim]
+    v_swa: np.ndarray                # [B, W, v_dim]
+    q_idx: Optional[np.ndarray] = None   # [B, HI, dI]  (Full / Reindex)
+    w_idx: Optional[np.ndarray] = None   # [B, HI] float32
+
+
+@dataclasses.dataclass
+class Workload:
+    name: str
+    shape: Shape
+    k_main: np.ndarray               # [B, N, k_dim]
+    v_main: np.ndarray               # [B, N, v_dim]
+    k_idx: np.ndarray                # [B, N, dI]
+    n_valid: np.ndarray              # [B] int32: valid compressed entries per query
+    n_swa: np.ndarray                # [B] int32: valid SWA rows (oldest first)
+    layers: List[Layer]
+    round_block_keys: int = 1        # block summary keys rounded to integers
+    note: str = ""
+
+
+def _rng(*key: int) -> np.random.Generator:
+    return np.random.default_rng(np.random.SeedSequence([int(k) for k in key]))
+
+
+def _normal_bf16(rng, shape, div):
+    x = rng.standard_normal(size=shape, dtype=np.float32)
+    if div != 1.0:
+        x *= np.float32(1.0 / div)
+    return f32_to_bf16_bits(x)
+
+
+def _int_bf16(rng, shape, lo=-4, hi=4):
+    x = rng.integers(lo, hi + 1, size=shape, dtype=np.int32).astype(np.float32)
+    return f32_to_bf16_bits(x)
+
+
+def _weights(rng, shape):
+    return rng.integers(1, 4, size=shape, dtype=np.int32).astype(np.float32)
+
+
+# mode patterns ---------------------------------------------------------------
+
+def encoder_group_modes(n_reuse: int = 5) -> List[int]:
+    """One encoder group: Full followed by ``n_reuse`` Reuse layers."""
+    return [FULL] + [REUSE] * n_reuse
+
+
+def decoder_group_modes() -> List[int]:
+    """Decoder stack: Full + 3 Reuse, then [Reindex + 3 Reuse] x 4 (20 layers)."""
+    return [FULL] + [REUSE] * 3 + ([REINDEX] + [REUSE] * 3) * 4
+
+
+def make_workload(shape: Shape, modes: List[int], *, seed: int = 0, cfg_id: int = 99,
+                  n_valid=None, n_swa=None, hier_full: int = 0, hier_reindex: int = 1,
+                  int_indexer: bool = True, name: str = "custom",
+                  round_block_keys: int = 1) -> Workload:
+    """Draw every tensor of a layer group.
+
+    ``seed`` and ``cfg_id`` select the stream; tensor ``t`` of layer ``l`` uses
+    the sub-stream (seed, cfg_id, t, l).  ``n_valid``/``n_swa`` default to
+    the full capacity; pass arrays (or callables of the rng) for ragged cases.
+    """
+    B, N = shape.batch, shape.n_entries
+    f32 = shape.dtype == "f32"
+
+    def kv(rng, shp, d):
+        if f32:
+            return rng.standard_normal(size=shp, dtype=np.float32)
+        return _normal_bf16(rng, shp, float(np.sqrt(d)))
+
+    def q_of(rng, shp):
+        if f32:
+            return rng.standard_normal(size=shp, dtype=np.float32)
+        return _normal_bf16(rng, shp, 1.0)
+
+    def idxv(rng, shp):
+        if f32 or not int_indexer:
+            x = rng.standard_normal(size=shp, dtype=np.float32)
+            return x if f32 else f32_to_bf16_bits(x)
+        return _int_bf16(rng, shp)
+
+    k_main = kv(_rng(seed, cfg_id, 1), (B, N, shape.k_dim), shape.k_dim)
+    v_main = kv(_rng(seed, cfg_id, 2), (B, N, shape.v_dim), shape.v_dim)
+    k_idx = idxv(_rng(seed, cfg_id, 3), (B, N, shape.idx_dim))
+    if n_valid is None:
+        n_valid = np.full(B, N, dtype=np.int32)
+    if n_swa is None:
+        n_swa = np.full(B, shape.swa, dtype=np.int32)
+    layers = []
+    for l, mode in enumerate(modes):
+        q = q_of(_rng(seed, cfg_id, 10, l), (B, shape.q_heads, shape.k_dim))
+        k_swa = kv(_rng(seed, cfg_id, 11, l), (B, shape.swa, shape.k_dim), shape.k_dim)
+        v_swa = kv(_rng(seed, cfg_id, 12, l), (B, shape.swa, shape.v_dim), shape.v_dim)
+        q_idx = w = None
+        if mode != REUSE:
+            q_idx = idxv(_rng(seed, cfg_id, 13, l), (B, shape.idx_heads, shape.idx_dim))
+            if f32:
+                w = np.ones((B, shape.idx_heads), dtype=np.float32)
+            else:
+                w = _weights(_rng(seed, cfg_id, 14, l), (B, shape.idx_heads))
+        hier = hier_full if mode == FULL else (hier_reindex if mode == REINDEX else 0)
+        if shape.pool_blocks <= 0:
+            hier = 0
+        layers.append(Layer(mode=mode, hier=hier, q=q, k_swa=k_swa, v_swa=v_swa,
+                            q_idx=q_idx, w_idx=w))
+    return Workload(name=name, shape=shape, k_main=k_main, v_main=v_main, k_idx=k_idx,
+                    n_valid=np.asarray(n_valid, dtype=np.int32),
+                    n_swa=np.asarray(n_swa, dtype=np.int32), layers=layers,
+                    round_block_keys=round_block_keys)
+
+
+def toy16(seed: int = 0) -> Workload:
+    """The page's 16-token illustration, with one compressed entry per token.
+
+    Token rows 0..15 carry K/V; the query sits at position 15.  The SWA
+    window holds the last 4 tokens (12..15) and the compressed candidates are
+    the tokens before it (0..11), so no token is attended twice.
+    """
+    T, W = 16, 4
+    shape = Shape(batch=1, n_entries=T, idx_heads=2, idx_dim=8, block=2, pool_blocks=4,
+                  topk=3, q_heads=4, k_dim=16, v_dim=16, swa=W, dtype="f32")
+    rng = _rng(seed, 0, 1)
+    k_tok = rng.standard_normal(size=(1, T, 16), dtype=np.float32)
+    v_tok = _rng(seed, 0, 2).standard_normal(size=(1, T, 16), dtype=np.float32)
+    k_idx = _rng(seed, 0, 3).standard_normal(size=(1, T, 8), dtype=np.float32)
+    q = _rng(seed, 0, 10).standard_normal(size=(1, 4, 16), dtype=np.float32)
+    q_idx = _rng(seed, 0, 13).standard_normal(size=(1, 2, 8), dtype=np.float32)
+    w = np.ones((1, 2), dtype=np.float32)
+    layer = Layer(mode=FULL, hier=1, q=q, k_swa=np.ascontiguousarray(k_tok[:, T - W:]),
+                  v_swa=np.ascontiguousarray(v_tok[:, T - W:]), q_idx=q_idx, w_idx=w)
+    return Workload(name="toy16", shape=shape, k_main=k_tok, v_main=v_tok, k_idx=k_idx,
+                    n_valid=np.array([T - W], dtype=np.int32),
+                    n_swa=np.array([W], dtype=np.int32), layers=[layer],
+                    round_block_keys=0,
+                    note="page-3 toy: 16 tokens, query at 15, Top-3, SWA 4, blocks of 2, pool 4")
+
+
+# named workloads -------------------------------------------------------------
+
+WORKLOADS = {
+    "toy16": dict(cfg_id=0),
+    "full_b8_8k": dict(cfg_id=1, batch=8, n_entries=2048, modes=[FULL], pool=0, context=8192),
+    "enc_b32_32k": dict(cfg_id=2, batch=32, n_entries=8192, modes=encoder_group_modes(5),
+                        pool=0, context=32768),
+    "reindex_b64_128k": dict(cfg_id=3, batch=64, n_entries=32768, modes=[REINDEX], pool=2048,
+                             context=131072),
+    "dec_b16_1m": dict(cfg_id=4, batch=16, n_entries=262144, modes=decoder_group_modes(),
+                       pool=2048, context=1048576),
+}
+
+
+def named(name: str, seed: int = 0, batch: Optional[int] = None) -> Workload:
+    """Build a named workload (optionally with a smaller batch for sampling)."""
+    if name == "toy16":
+        return toy16(seed)
+    spec = WORKLOADS[name]
+    shape = Shape(batch=batch or spec["batch"], n_entries=spec["n_entries"],
+                  pool_blocks=spec["pool"])
+    wl = make_workload(shape, spec["modes"], seed=seed, cfg_id=spec["cfg_id"], name=name)
+    wl.note = f"{spec['context']} tokens at ratio 4"
+    return wl

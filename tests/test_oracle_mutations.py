@@ -1,0 +1,95 @@
+"""The oracle's pins catch plausible mistakes.
+
+Each case plants one slip in the oracle (on the CPU, through monkeypatch) and
+checks that at least one pin of ``test_oracle_pins`` fails with it.
+"""
+import numpy as np
+import pytest
+
+import oracle
+import oracle.csa2 as C
+from tests import test_oracle_pins as P
+
+PINS = [P.test_golden_toy16_hand, P.test_indexer_scores_match_integer_loops,
+        P.test_block_keys_rounding_half_even_and_partial_block,
+        P.test_topk_matches_heap_selection_with_ties, P.test_topk_special_cases,
+        P.test_hierarchical_equals_flat_when_pool_covers_every_block,
+        P.test_reuse_layers_return_the_indexing_layers_indices,
+        P.test_attention_closed_forms, P.test_toy16_structure,
+        lambda: P.test_sparse_equals_dense_causal_attention_naive(24, 8, 16)]
+
+
+def _topk_highest_id_wins(scores, ids, k):
+    scores = np.where(np.isnan(scores), -np.inf, scores)
+    order = np.lexsort((-ids, -scores))
+    chosen = np.sort(ids[order[:min(k, len(ids))]])
+    out = np.full(k, -1, dtype=np.int64)
+    out[:len(chosen)] = chosen
+    return out
+
+
+def _scores_without_relu(q_idx, w, keys, relu=True):
+    return (keys @ q_idx.T) @ w
+
+
+def _scores_without_weights(q_idx, w, keys, relu=True):
+    d = keys @ q_idx.T
+    return (np.maximum(d, 0.0) if relu else d).sum(axis=1)
+
+
+def _block_keys_half_up(keys, n_valid, block, round_to_int, store_bf16=False):
+    nb = -(-n_valid // block)
+    out = np.zeros((nb, keys.shape[1]))
+    for j in range(nb):
+        rows = keys[j * block: min((j + 1) * block, n_valid)]
+        m = rows.sum(axis=0) / rows.shape[0]
+        out[j] = np.floor(m + 0.5) if round_to_int else m
+    return out
+
+
+def _attention_without_swa(q, k_main, v_main, idx, k_swa, v_swa, n_swa, scale):
+    sel = idx[idx >= 0]
+    return C.attend(q, k_main[sel], v_main[sel], scale)
+
+
+def _attend_without_scale(q, k_rows, v_rows, scale):
+    return _orig_attend(q, k_rows, v_rows, 1.0)
+
+
+def _pooled_entries_off_by_one(pool, n_valid, block):
+    ent = (pool[:, None] * block + 1 + np.arange(block)[None, :]).reshape(-1)
+    return ent[ent < n_valid]
+
+
+def _pool_unsorted(q_idx, w, kb, n_blocks, pool, relu=True):
+    s = C.indexer_scores(q_idx, w, kb[:n_blocks], relu)
+    order = np.lexsort((np.arange(n_blocks), -s))
+    return order[:min(pool, n_blocks)]
+
+
+_orig_attend = C.attend
+
+MUTATIONS = {
+    "tie-break keeps the highest id": ("select_topk", _topk_highest_id_wins),
+    "ReLU dropped": ("indexer_scores", _scores_without_relu),
+    "head weights dropped": ("indexer_scores", _scores_without_weights),
+    "block keys rounded half up": ("block_keys", _block_keys_half_up),
+    "SWA rows dropped": ("sparse_attention", _attention_without_swa),
+    "softmax scale dropped": ("attend", _attend_without_scale),
+    "pooled entries shifted by one": ("pooled_entries", _pooled_entries_off_by_one),
+    "pool left in score order": ("pool_blocks", _pool_unsorted),
+}
+
+
+@pytest.mark.parametrize("name", sorted(MUTATIONS))
+def test_planted_mistake_fails_a_pin(name, monkeypatch):
+    fn, bad = MUTATIONS[name]
+    monkeypatch.setattr(C, fn, bad)
+    monkeypatch.setattr(oracle, fn, bad)
+    failed = []
+    for pin in PINS:
+        try:
+            pin()
+        except (AssertionError, ValueError, IndexError):
+            failed.append(getattr(pin, "__name__", "pin"))
+    assert failed, f"no pin caught: {name}"

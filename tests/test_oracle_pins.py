@@ -1,0 +1,290 @@
+"""Pins for the CPU oracle: checks against things the pages and mathematics fix.
+
+None of these compares the oracle with itself.  Each check would fail on a
+plausible slip in the oracle (dropped ReLU or weight, wrong tie-break
+direction, transposed operand, missing SWA rows, wrong softmax scale, wrong
+rounding mode, pool not sorted, Reuse recomputing its indices).
+"""
+import heapq
+import json
+import math
+import os
+
+import numpy as np
+import pytest
+
+import oracle
+from oracle import FULL, REINDEX, REUSE
+from sparse_attention_decode_index_gb300 import workloads as W
+
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+
+
+def _load(name):
+    with open(os.path.join(GOLDEN, name)) as f:
+        return json.load(f)
+
+
+# ---------------------------------------------------------------- hand-worked toy
+
+def test_golden_toy16_hand():
+    g = _load("toy16_hand.json")
+    keys = np.array(g["keys"], dtype=np.float64)[:, None]
+    q = np.ones((1, 1))
+    w = np.ones(1)
+    n_valid, blk, pool, k = g["n_valid"], g["block"], g["pool"], g["topk"]
+
+    kb_unr = oracle.block_keys(keys, n_valid, blk, round_to_int=False)
+    kb_r = oracle.block_keys(keys, n_valid, blk, round_to_int=True)
+    assert kb_unr[:, 0].tolist() == g["block_means"]
+    assert kb_r[:, 0].tolist() == g["block_keys_rounded"]
+    assert oracle.indexer_scores(q, w, kb_r).tolist() == g["block_scores_rounded"]
+
+    nb = len(g["block_means"])
+    assert oracle.pool_blocks(q, w, kb_r, nb, pool).tolist() == g["pool_rounded"]
+    assert oracle.pool_blocks(q, w, kb_unr, nb, pool).tolist() == g["pool_unrounded"]
+
+    r = oracle.layer_indices(q, w, keys, kb_r, n_valid, topk=k, block=blk, pool=pool, hier=True)
+    assert r["cand"].tolist() == g["candidates_rounded"]
+    assert r["scores"].tolist() == g["candidate_scores_rounded"]
+    assert r["idx"].tolist() == g["top3_hier_rounded"]
+    r = oracle.layer_indices(q, w, keys, kb_unr, n_valid, topk=k, block=blk, pool=pool, hier=True)
+    assert r["idx"].tolist() == g["top3_hier_unrounded"]
+    r = oracle.layer_indices(q, w, keys, None, n_valid, topk=k, block=blk, pool=pool, hier=False)
+    assert r["idx"].tolist() == g["top3_flat"]
+
+    # attention reads the 3 selected entries plus the 4 window tokens
+    n_keys = int((r["idx"] >= 0).sum()) + g["swa"]
+    assert n_keys == g["attended_keys"]
+
+
+def test_toy16_structure():
+    """Counts fixed by the page's toy: 12 candidates -> 6 blocks -> pool 4 -> 8 -> Top-3, 7 keys."""
+    for seed in range(5):
+        wl = W.toy16(seed)
+        res = oracle.run_group(wl)
+        r = res[0]
+        assert int(wl.n_valid[0]) == 12 and int(wl.n_swa[0]) == 4
+        assert len(r["pool"][0]) == 4
+        assert len(r["cand"][0]) == 8
+        idx = r["idx"][0]
+        assert (idx >= 0).sum() == 3 and np.all(idx[idx >= 0] < 12)
+        assert np.all(np.diff(idx) > 0)
+        assert set(idx.tolist()) <= set(r["cand"][0].tolist())
+        assert r["out"].shape == (1, 4, 16)
+
+
+# ---------------------------------------------------------------- indexer
+
+def test_indexer_scores_match_integer_loops():
+    rng = np.random.default_rng(7)
+    for relu in (True, False):
+        for _ in range(20):
+            HI, dI, n = rng.integers(1, 5), rng.integers(1, 9), rng.integers(1, 12)
+            q = rng.integers(-4, 5, size=(HI, dI))
+            k = rng.integers(-4, 5, size=(n, dI))
+            w = rng.integers(1, 4, size=HI)
+            want = []
+            for j in range(n):
+                s = 0
+                for h in range(HI):
+                    d = sum(int(q[h, i]) * int(k[j, i]) for i in range(dI))
+                    if relu and d < 0:
+                        d = 0
+                    s += int(w[h]) * d
+                want.append(s)
+            got = oracle.indexer_scores(q.astype(np.float64), w.astype(np.float64),
+                                        k.astype(np.float64), relu)
+            assert got.tolist() == [float(x) for x in want]
+
+
+def test_block_keys_rounding_half_even_and_partial_block():
+    # blocks of 2: sums 1, 3, -1, -3, 5 -> means .5, 1.5, -.5, -1.5, 2.5 -> 0, 2, -0, -2, 2
+    keys = np.array([0, 1, 1, 2, 0, -1, -1, -2, 2, 3, 7], dtype=np.float64)[:, None]
+    kb = oracle.block_keys(keys, 11, 2, round_to_int=True)
+    assert kb[:, 0].tolist() == [0.0, 2.0, 0.0, -2.0, 2.0, 7.0]    # last block holds entry 10 only
+    kb = oracle.block_keys(keys, 9, 2, round_to_int=False)
+    assert kb[:, 0].tolist() == [0.5, 1.5, -0.5, -1.5, 2.0]      # n_valid = 9: last block = entry 8
+
+
+def test_bf16_decode_and_rounding():
+    bits = np.array([0x3F80, 0xC000, 0x3FC0, 0x0000, 0x4080, 0xBE00], dtype=np.uint16)
+    assert oracle.to_f64(bits).tolist() == [1.0, -2.0, 1.5, 0.0, 4.0, -0.125]
+    # 1 + 2^-8 is halfway between 1 and 1 + 2^-7 -> even (1); 1 + 3*2^-8 -> 1 + 2^-6
+    x = np.array([1 + 2 ** -8, 1 + 3 * 2 ** -8, 3.0, -(1 + 2 ** -8), 1 + 2 ** -9])
+    assert oracle.round_bf16(x).tolist() == [1.0, 1 + 2 ** -6, 3.0, -1.0, 1.0]
+    # the generator's rounding agrees with the oracle's decoding on exact values
+    v = np.array([1.0, -2.0, 0.5, 3.0, -4.0], dtype=np.float32)
+    assert oracle.to_f64(W.f32_to_bf16_bits(v)).tolist() == v.tolist()
+
+
+# ---------------------------------------------------------------- Top-K
+
+def _heap_topk(scores, ids, k):
+    """Independent selection: k smallest of (-score, id) with heapq."""
+    s = [(-math.inf if math.isnan(x) else x) for x in scores]
+    best = heapq.nsmallest(min(k, len(ids)), zip([-x for x in s], ids))
+    out = sorted(i for _, i in best)
+    return out + [-1] * (k - len(out))
+
+
+def test_topk_matches_heap_selection_with_ties():
+    rng = np.random.default_rng(11)
+    for _ in range(300):
+        n = int(rng.integers(0, 40))
+        k = int(rng.integers(1, 45))
+        scores = rng.integers(-3, 4, size=n).astype(np.float64)
+        ids = np.sort(rng.choice(1000, size=n, replace=False))
+        assert oracle.select_topk(scores, ids, k).tolist() == _heap_topk(scores.tolist(), ids.tolist(), k)
+
+
+def test_topk_special_cases():
+    ids = np.arange(10)
+    # all equal: the lowest ids win
+    assert oracle.select_topk(np.zeros(10), ids, 4).tolist() == [0, 1, 2, 3]
+    # k >= n: everything, padded with -1
+    assert oracle.select_topk(np.arange(3.0), np.arange(3), 5).tolist() == [0, 1, 2, -1, -1]
+    # strict order: the largest scores, returned in ascending id order
+    assert oracle.select_topk(np.array([1.0, 9, 3, 7, 5]), np.arange(5), 2).tolist() == [1, 3]
+    # NaN ranks like -inf (below every finite score; ties with -inf by id)
+    s = np.array([np.nan, -np.inf, 0.0, np.nan])
+    assert oracle.select_topk(s, np.arange(4), 2).tolist() == [0, 2]
+
+
+# ---------------------------------------------------------------- hierarchy / modes
+
+def _group(shape, modes, n_valid, seed=3, hier_full=0):
+    return W.make_workload(shape, modes, seed=seed, n_valid=n_valid, hier_full=hier_full)
+
+
+def test_hierarchical_equals_flat_when_pool_covers_every_block():
+    for relu in (1, 0):
+        sh = W.Shape(batch=3, n_entries=104, idx_heads=3, idx_dim=8, block=8, pool_blocks=13,
+                     topk=20, q_heads=2, k_dim=8, v_dim=4, swa=4, relu=relu)
+        wl_h = _group(sh, [FULL], n_valid=[104, 97, 1], hier_full=1)
+        wl_f = _group(sh, [FULL], n_valid=[104, 97, 1], hier_full=0)
+        rh = oracle.run_group(wl_h, want_attention=False)[0]
+        rf = oracle.run_group(wl_f, want_attention=False)[0]
+        assert np.array_equal(rh["idx"], rf["idx"])
+        # and a smaller pool does restrict the candidates to 8 * pool entries
+        sh2 = W.Shape(**{**sh.__dict__, "pool_blocks": 3})
+        r2 = oracle.run_group(_group(sh2, [FULL], n_valid=[104, 97, 1], hier_full=1),
+                              want_attention=False)[0]
+        assert len(r2["cand"][0]) == 24 and len(r2["cand"][2]) == 1
+
+
+def test_reuse_layers_return_the_indexing_layers_indices():
+    sh = W.Shape(batch=2, n_entries=64, idx_heads=2, idx_dim=8, block=8, pool_blocks=4,
+                 topk=6, q_heads=2, k_dim=8, v_dim=4, swa=4)
+    wl = W.make_workload(sh, [FULL, REUSE, REUSE, REINDEX, REUSE], seed=5)
+    res = oracle.run_group(wl)
+    assert np.array_equal(res[1]["idx"], res[0]["idx"])
+    assert np.array_equal(res[2]["idx"], res[0]["idx"])
+    assert np.array_equal(res[4]["idx"], res[3]["idx"])
+    # each layer still uses its own query: outputs differ between Full and Reuse
+    assert not np.allclose(res[0]["out"], res[1]["out"])
+    with pytest.raises(ValueError):
+        oracle.run_group(W.make_workload(sh, [REUSE], seed=5))
+
+
+def test_group_counts_of_the_40_layer_pattern():
+    enc = ["swa", "swa"] + W.encoder_group_modes(5) * 3
+    dec = W.decoder_group_modes()
+    assert len(enc) == 20 and len(dec) == 20
+    c = oracle.group_counts(enc + dec)
+    assert c == {"layers": 40, "csa2": 38, "kv_storing": 4, "indexers": 8}
+    assert REINDEX not in enc
+
+
+# ---------------------------------------------------------------- attention
+
+def _naive_dense(q, k, v, scale):
+    """Textbook attention with python loops (fp64)."""
+    H, dv = len(q), len(v[0])
+    out, lse = [], []
+    for h in range(H):
+        logits = [scale * sum(q[h][i] * k[j][i] for i in range(len(q[h]))) for j in range(len(k))]
+        m = max(logits)
+        e = [math.exp(x - m) for x in logits]
+        s = sum(e)
+        out.append([sum(e[j] * v[j][c] for j in range(len(k))) / s for c in range(dv)])
+        lse.append(m + math.log(s))
+    return np.array(out), np.array(lse)
+
+
+def _ratio1_case(T, Wn, K, H, dk, dv, seed):
+    """Ratio-1 sequence of T tokens; query at T-1; entries 0..T-1-W, window the rest."""
+    rng = np.random.default_rng(seed)
+    k_tok = rng.standard_normal((T, dk))
+    v_tok = rng.standard_normal((T, dv))
+    q = rng.standard_normal((H, dk))
+    q_idx = rng.integers(-4, 5, size=(2, 4)).astype(np.float64)
+    k_idx = rng.integers(-4, 5, size=(T, 4)).astype(np.float64)
+    n_swa = min(Wn, T)
+    n_valid = T - n_swa
+    return k_tok, v_tok, q, q_idx, k_idx, n_valid, n_swa
+
+
+@pytest.mark.parametrize("T,Wn,K", [(24, 8, 16), (9, 8, 16), (5, 8, 4), (16, 4, 12)])
+def test_sparse_equals_dense_causal_attention_naive(T, Wn, K):
+    k_tok, v_tok, q, q_idx, k_idx, n_valid, n_swa = _ratio1_case(T, Wn, K, 3, 5, 4, T)
+    sel = oracle.layer_indices(q_idx, np.ones(2), k_idx, None, n_valid, topk=K, block=2, pool=0,
+                               hier=False)["idx"]
+    scale = 1 / math.sqrt(5)
+    out, lse = oracle.sparse_attention(q, k_tok, v_tok, sel, k_tok[n_valid:], v_tok[n_valid:],
+                                       n_swa, scale)
+    ref_out, ref_lse = _naive_dense(q.tolist(), k_tok.tolist(), v_tok.tolist(), scale)
+    assert np.allclose(out, ref_out, rtol=0, atol=1e-12)
+    assert np.allclose(lse, ref_lse, rtol=0, atol=1e-12)
+
+
+def test_sparse_equals_dense_attention_sdpa_at_512_plus_128():
+    torch = pytest.importorskip("torch")
+    T, Wn, K, H, dk, dv = 640, 128, 512, 4, 192, 128
+    k_tok, v_tok, q, q_idx, k_idx, n_valid, n_swa = _ratio1_case(T, Wn, K, H, dk, dv, 1)
+    sel = oracle.layer_indices(q_idx, np.ones(2), k_idx, None, n_valid, topk=K, block=8, pool=0,
+                               hier=False)["idx"]
+    assert (sel >= 0).sum() == 512
+    out, lse = oracle.sparse_attention(q, k_tok, v_tok, sel, k_tok[n_valid:], v_tok[n_valid:],
+                                       n_swa, 1 / math.sqrt(dk))
+    qt = torch.tensor(q)[:, None, :]                    # [H, 1, dk]
+    kt = torch.tensor(k_tok)[None].expand(H, T, dk)
+    vt = torch.tensor(v_tok)[None].expand(H, T, dv)
+    ref = torch.nn.functional.scaled_dot_product_attention(qt, kt, vt)[:, 0, :].numpy()
+    assert np.allclose(out, ref, rtol=0, atol=1e-12)
+    ref_lse = torch.logsumexp(torch.einsum("hd,td->ht", torch.tensor(q), torch.tensor(k_tok))
+                              / math.sqrt(dk), dim=1).numpy()
+    assert np.allclose(lse, ref_lse, rtol=0, atol=1e-12)
+
+
+def test_attention_closed_forms():
+    rng = np.random.default_rng(2)
+    H, dk, dv, N = 3, 6, 5, 30
+    k_main = rng.standard_normal((N, dk))
+    v_main = rng.standard_normal((N, dv))
+    k_swa = rng.standard_normal((4, dk))
+    v_swa = rng.standard_normal((4, dv))
+    idx = np.array([3, 7, 19, -1, -1])
+    # q = 0: uniform weights -> mean of the attended V rows, lse = log(n)
+    out, lse = oracle.sparse_attention(np.zeros((H, dk)), k_main, v_main, idx, k_swa, v_swa, 4, 0.7)
+    want = np.concatenate([v_main[[3, 7, 19]], v_swa]).mean(axis=0)
+    assert np.allclose(out, want[None, :], atol=1e-13) and np.allclose(lse, math.log(7))
+    # a single attended key -> its V row, lse = scale * q.k
+    q = rng.standard_normal((H, dk))
+    out, lse = oracle.sparse_attention(q, k_main, v_main, np.array([11, -1]), k_swa, v_swa, 0, 0.3)
+    assert np.allclose(out, v_main[11][None, :], atol=1e-13)
+    assert np.allclose(lse, 0.3 * q @ k_main[11], atol=1e-13)
+    # no key at all -> zero output, lse = -inf
+    out, lse = oracle.sparse_attention(q, k_main, v_main, np.array([-1]), k_swa, v_swa, 0, 0.3)
+    assert np.all(out == 0) and np.all(np.isneginf(lse))
+    # invariance under a permutation of the cache rows (indices remapped)
+    perm = rng.permutation(N)
+    inv = np.argsort(perm)
+    idx = np.array([0, 5, 9, 28])
+    a, la = oracle.sparse_attention(q, k_main, v_main, idx, k_swa, v_swa, 4, 0.4)
+    b, lb = oracle.sparse_attention(q, k_main[perm], v_main[perm], inv[idx], k_swa, v_swa, 4, 0.4)
+    assert np.allclose(a, b, atol=1e-13) and np.allclose(la, lb, atol=1e-13)
+    # the softmax scale multiplies the logits (a doubled scale != the original)
+    c, _ = oracle.sparse_attention(q, k_main, v_main, idx, k_swa, v_swa, 4, 0.8)
+    assert not np.allclose(a, c)
