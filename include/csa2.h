@@ -1,0 +1,209 @@
+/*
+ * csa2.h -- C ABI of libcsa2.so: CSA2 sparse decode attention on one GB300.
+ *
+ * The method (DeepSeek V4.1 Flash, as described on the architecture page
+ * k-a.in "DeepSeek V4.1 Flash"):
+ *   - section "CSA2 with cross-layer reuse", mode table: a Full layer computes
+ *     its own main KV / indexer keys and a fresh Top-K; a Reindex layer reuses
+ *     them but runs its own indexer query and a fresh Top-K; a Reuse layer
+ *     reuses KV, indexer keys and the Top-K indices.  Every mode computes its
+ *     own main query and SWA KV.
+ *   - bullet "Sparse attention": each query reads its Top-512 main-KV entries
+ *     plus a 128-token sliding window (SWA).
+ *   - bullet "Hierarchical indexer": later decoder indexers score at most
+ *     16,384 candidates whatever the context length (blocks of 8 entries, a
+ *     pool of at most 2,048 blocks); page "DeepSeek V4.1 Flash made encoders
+ *     cool" (artofsm.art): the hierarchical sparse indexer narrows candidates
+ *     to blocks.
+ * The pages do not give the indexer formula (they point to "section 4.2.1" of
+ * a report that is not among them).  This library computes, for a query with
+ * indexer heads q_h and weights w_h, the score of a key k as
+ *     s(k) = sum_h w_h * ReLU(q_h . k)          (ReLU optional, see relu)
+ * and selects Top-K under the total order (score descending, index ascending).
+ *
+ * Conventions shared by every entry point
+ *   - Every pointer argument is DEVICE memory owned by the caller, row-major
+ *     and contiguous, unless stated otherwise.  Arrays read by bulk copies
+ *     (keys, main KV, SWA KV, queries) must be 16-byte aligned.
+ *   - Work is enqueued on `stream` (a cudaStream_t; NULL = legacy default
+ *     stream).  No entry point allocates or frees memory, and none
+ *     synchronises except csa2_read_device_error.
+ *   - Arguments are validated on the host before anything is enqueued; a
+ *     negative csa2_status is returned and nothing is launched.  A failed
+ *     launch returns CSA2_ERR_CUDA.
+ *   - Conditions only the device can see (an index outside the cache, a count
+ *     outside its range, a pooled block id outside the valid blocks) are
+ *     clamped or skipped by the kernels and recorded in a sticky error word in
+ *     the workspace header; kernels never trap.  Read it with
+ *     csa2_read_device_error.
+ *   - `ws` is a caller-owned device workspace of at least
+ *     csa2_workspace_bytes(shape) bytes, 256-byte aligned, zeroed once with
+ *     csa2_workspace_init before first use.  Calls that share a workspace
+ *     must be ordered on one stream.
+ *   - Element type (csa2_shape.dtype): bf16 or fp32, for queries, keys,
+ *     values and indexer tensors alike.  Scores, weights, outputs and lse are
+ *     fp32; indices and counts are int32.
+ */
+#ifndef CSA2_H_
+#define CSA2_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct CUstream_st* csa2_stream_t; /* identical to cudaStream_t */
+
+typedef enum {
+  CSA2_OK = 0,
+  CSA2_ERR_INVALID_ARG = -1,  /* null pointer, bad size, misaligned pointer, illegal mode sequence */
+  CSA2_ERR_UNSUPPORTED = -2,  /* valid but not implemented (e.g. dims beyond the generic limits) */
+  CSA2_ERR_WORKSPACE = -3,    /* ws too small or misaligned */
+  CSA2_ERR_CUDA = -4,         /* a CUDA launch or runtime call failed */
+  CSA2_ERR_DEVICE_CHECK = -5, /* returned by csa2_read_device_error: a kernel recorded a bad input */
+  CSA2_ERR_TIMEOUT = -6       /* returned by csa2_read_device_error: a bounded device wait gave up */
+} csa2_status;
+
+typedef enum { CSA2_FULL = 0, CSA2_REINDEX = 1, CSA2_REUSE = 2 } csa2_mode;
+typedef enum { CSA2_BF16 = 0, CSA2_F32 = 1 } csa2_dtype;
+
+/* Problem shape shared by a layer group.  Symbols: B batch (one decode query
+ * per sequence), N compressed main-KV entries per sequence (cache capacity),
+ * HI x dI indexer heads x dim, P pool blocks, K Top-K, H query heads sharing
+ * one KV head with key dim dk and value dim dv, W SWA rows. */
+typedef struct {
+  int32_t batch;       /* B >= 1 */
+  int32_t n_entries;   /* N >= 1; a multiple of `block` when a hierarchical stage is used */
+  int32_t idx_heads;   /* HI, 1..64 */
+  int32_t idx_dim;     /* dI, 1..1024 */
+  int32_t block;       /* entries per block, >= 1 (8 in the architecture) */
+  int32_t pool_blocks; /* P: blocks kept by the hierarchical stage; 0 = no hierarchical stage */
+  int32_t topk;        /* K, 1..1024 (512 in the architecture) */
+  int32_t q_heads;     /* H, 1..1024 */
+  int32_t k_dim;       /* dk, 1..1024 */
+  int32_t v_dim;       /* dv, 1..1024 */
+  int32_t swa;         /* W, 0..1024 (128 in the architecture); K + W <= 1024 */
+  float scale;         /* softmax scale; <= 0 selects 1/sqrt(dk) */
+  int32_t relu;        /* 1: ReLU on each indexer head's dot product (default reading); 0: none */
+  int32_t dtype;       /* csa2_dtype */
+} csa2_shape;
+
+/* One layer of a group (csa2_layer_group). */
+typedef struct {
+  int32_t mode;        /* csa2_mode */
+  int32_t hier;        /* 1: hierarchical (block pool) indexing; needs kb and pool_blocks > 0 */
+  const void* q;       /* [B, H, dk] the layer's own query */
+  const void* q_idx;   /* [B, HI, dI] indexer query (Full / Reindex; ignored for Reuse) */
+  const float* w_idx;  /* [B, HI] indexer head weights (Full / Reindex; ignored for Reuse) */
+  const void* k_swa;   /* [B, W, dk] the layer's own SWA keys, oldest first */
+  const void* v_swa;   /* [B, W, dv] the layer's own SWA values */
+  float* out;          /* [B, H, dv] attention output */
+  float* lse;          /* [B, H] natural-log sum of exp of the scaled logits, or NULL */
+  int32_t* idx_out;    /* [B, K] fresh indices of an indexing layer, or NULL; untouched for Reuse */
+} csa2_layer;
+
+/* Workspace bytes needed by any entry point for this shape (host only). */
+size_t csa2_workspace_bytes(const csa2_shape* shape);
+
+/* Zero the workspace header (device error word).  Call once before first use. */
+int csa2_workspace_init(void* ws, size_t ws_bytes, csa2_stream_t stream);
+
+/* Block summary keys (cache-side maintenance, architecture page bullet
+ * "Hierarchical indexer"; the 128K Reindex workload defines the summary as
+ * the mean of the block's 8 keys rounded to integers).
+ * kb[b, j, :] = mean of k_idx[b, j*block + t, :] over the valid entries
+ * t < block with j*block + t < n_valid[b] (a partial last block averages its
+ * valid entries), rounded half-to-even to an integer if round_to_int, then
+ * stored in the element type.  Blocks j >= ceil(n_valid[b] / block) are
+ * written as 0.
+ *   k_idx   [B, N, dI]     n_valid [B] (0..N)
+ *   kb      [B, ceil(N / block), dI]  (output) */
+int csa2_block_keys(const csa2_shape* shape, const void* k_idx, const int32_t* n_valid,
+                    int32_t round_to_int, void* kb, void* ws, size_t ws_bytes, csa2_stream_t stream);
+
+/* Hierarchical first stage: score every valid block summary key with the
+ * indexer formula and keep the top min(P, NB_b) blocks, NB_b = ceil(n_valid[b] / block),
+ * under (block score descending, block id ascending).
+ *   q_idx [B, HI, dI]   w [B, HI]   kb [B, ceil(N / block), dI]   n_valid [B]
+ *   pool_out   [B, P]  (output) pooled block ids in ascending order, padded with -1
+ *   n_pool_out [B]     (output) min(P, NB_b) */
+int csa2_index_blocks(const csa2_shape* shape, const void* q_idx, const float* w, const void* kb,
+                      const int32_t* n_valid, int32_t* pool_out, int32_t* n_pool_out, void* ws,
+                      size_t ws_bytes, csa2_stream_t stream);
+
+/* Token-level indexer scores.
+ * Flat (pool == NULL): scores_out[b, j] = s(k_idx[b, j]) for j < n_valid[b];
+ *   cand_out (nullable) receives j; n_cand_out (nullable) receives n_valid[b].
+ *   scores_out / cand_out have row stride N.
+ * Pooled (pool != NULL, from csa2_index_blocks): the candidates are the
+ *   entries of the pooled blocks in pool order (ascending entry id);
+ *   position p*block + t holds entry pool[b, p]*block + t, its score, or
+ *   cand -1 / score -inf when that entry is >= n_valid[b].
+ *   scores_out / cand_out have row stride P*block; n_cand_out[b] = n_pool[b]*block.
+ *   cand_out and n_cand_out are required. */
+int csa2_index_tokens(const csa2_shape* shape, const void* q_idx, const float* w, const void* k_idx,
+                      const int32_t* n_valid, const int32_t* pool, const int32_t* n_pool,
+                      float* scores_out, int32_t* cand_out, int32_t* n_cand_out, void* ws,
+                      size_t ws_bytes, csa2_stream_t stream);
+
+/* Exact Top-k of each row: scores [B, ld] (row stride ld), optional candidate
+ * ids cand [B, ld] (NULL: the id is the position; ids < 0 are skipped; ids
+ * must ascend with position), n_cand [B] positions to consider (NULL: ld).
+ * Order: score descending, id ascending; -0 equals +0 and NaN ranks as -inf.
+ *   idx_out   [B, k] (output) selected ids in ascending order, padded with -1
+ *   score_out [B, k] (output, nullable) their scores (-inf for padding)
+ * 1 <= k <= 16384, ld <= 2^28. */
+int csa2_topk(const csa2_shape* shape, const float* scores, int32_t ld, const int32_t* cand,
+              const int32_t* n_cand, int32_t k, int32_t* idx_out, float* score_out, void* ws,
+              size_t ws_bytes, csa2_stream_t stream);
+
+/* Sparse attention of one decode query per sequence (all H heads share one
+ * KV head): one softmax over the main-KV rows idx[b, :] (entries < 0 are
+ * skipped) and the SWA rows 0..n_swa[b]-1.
+ *   q [B, H, dk]  k_main [B, N, dk]  v_main [B, N, dv]  idx [B, K]
+ *   k_swa [B, W, dk]  v_swa [B, W, dv]  n_swa [B] (0..W)
+ *   out [B, H, dv] (output)  lse [B, H] (output, nullable; -inf and out = 0
+ *   when a query attends no row at all). */
+int csa2_sparse_attn(const csa2_shape* shape, const void* q, const void* k_main, const void* v_main,
+                     const int32_t* idx, const void* k_swa, const void* v_swa, const int32_t* n_swa,
+                     float* out, float* lse, void* ws, size_t ws_bytes, csa2_stream_t stream);
+
+/* A whole layer group over one shared main KV and indexer-key cache (the
+ * group's Full layer's): layers run in order; Full and Reindex compute fresh
+ * indices (flat, or hierarchical when layer.hier), Reuse attends with the
+ * latest indices; every layer attends with its own q and SWA KV.
+ * Rules: a Reuse layer needs an earlier Full or Reindex layer in the group;
+ * hier needs kb (from csa2_block_keys) and pool_blocks > 0.
+ *   k_main [B, N, dk]  v_main [B, N, dv]  k_idx [B, N, dI]
+ *   kb [B, ceil(N / block), dI] (nullable when no layer is hierarchical)
+ *   n_valid [B] (0..N)  n_swa [B] (0..W) */
+int csa2_layer_group(const csa2_shape* shape, const csa2_layer* layers, int32_t n_layers,
+                     const void* k_main, const void* v_main, const void* k_idx, const void* kb,
+                     const int32_t* n_valid, const int32_t* n_swa, void* ws, size_t ws_bytes,
+                     csa2_stream_t stream);
+
+/* Static description of a status code. */
+const char* csa2_status_str(int status);
+
+/* Synchronise `stream`, read and clear the sticky device error word of `ws`.
+ * Returns CSA2_OK, CSA2_ERR_DEVICE_CHECK or CSA2_ERR_TIMEOUT (a bounded wait
+ * gave up); *detail (nullable) receives the error bits (bit 0 bad index,
+ * bit 1 bad count, bit 2 timeout, bit 3 bad pooled block) in its low byte. */
+int csa2_read_device_error(void* ws, csa2_stream_t stream, int32_t* detail);
+
+/* 1 when the fast (tensor-core) kernels serve this shape, 0 when the generic
+ * kernels do (host only; for diagnostics and tests). */
+int csa2_fast_path(const csa2_shape* shape, int32_t* indexer_fast, int32_t* attention_fast);
+
+/* Number of kernel launches this library has enqueued since it was loaded
+ * (all threads and devices; launches recorded into a CUDA graph count once,
+ * at capture).  For diagnostics and launch accounting. */
+unsigned long long csa2_launch_count(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* CSA2_H_ */

@@ -1,0 +1,300 @@
+"""Python binding of libcsa2.so (ctypes).
+
+Argument marshalling only: every step of the computation runs in the
+library's CUDA kernels.  Functions take torch CUDA tensors (PyTorch supplies
+device memory and streams) and mirror the C entry points of ``csa2.h``
+without the ``csa2_`` prefix.  The library is loaded on first use and a
+missing build raises immediately; there is no fallback implementation.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from typing import Iterable, Optional, Sequence
+
+import torch
+
+HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(HERE, "libcsa2.so")
+
+FULL, REINDEX, REUSE = 0, 1, 2
+BF16, F32 = 0, 1
+
+OK = 0
+STATUS = {0: "CSA2_OK", -1: "CSA2_ERR_INVALID_ARG", -2: "CSA2_ERR_UNSUPPORTED", -3: "CSA2_ERR_WORKSPACE",
+          -4: "CSA2_ERR_CUDA", -5: "CSA2_ERR_DEVICE_CHECK", -6: "CSA2_ERR_TIMEOUT"}
+
+
+class CSA2Error(RuntimeError):
+    def __init__(self, status: int, what: str):
+        self.status = status
+        super().__init__(f"{what}: {STATUS.get(status, status)} ({status_str(status)})")
+
+
+class CShape(ctypes.Structure):
+    _fields_ = [("batch", ctypes.c_int32), ("n_entries", ctypes.c_int32), ("idx_heads", ctypes.c_int32),
+                ("idx_dim", ctypes.c_int32), ("block", ctypes.c_int32), ("pool_blocks", ctypes.c_int32),
+                ("topk", ctypes.c_int32), ("q_heads", ctypes.c_int32), ("k_dim", ctypes.c_int32),
+                ("v_dim", ctypes.c_int32), ("swa", ctypes.c_int32), ("scale", ctypes.c_float),
+                ("relu", ctypes.c_int32), ("dtype", ctypes.c_int32)]
+
+
+class CLayer(ctypes.Structure):
+    _fields_ = [("mode", ctypes.c_int32), ("hier", ctypes.c_int32), ("q", ctypes.c_void_p),
+                ("q_idx", ctypes.c_void_p), ("w_idx", ctypes.c_void_p), ("k_swa", ctypes.c_void_p),
+                ("v_swa", ctypes.c_void_p), ("out", ctypes.c_void_p), ("lse", ctypes.c_void_p),
+                ("idx_out", ctypes.c_void_p)]
+
+
+_lib = None
+_VP, _I32, _SZ = ctypes.c_void_p, ctypes.c_int32, ctypes.c_size_t
+_SIGS = {
+    "csa2_workspace_bytes": (_SZ, [ctypes.POINTER(CShape)]),
+    "csa2_workspace_init": (ctypes.c_int, [_VP, _SZ, _VP]),
+    "csa2_block_keys": (ctypes.c_int, [ctypes.POINTER(CShape), _VP, _VP, _I32, _VP, _VP, _SZ, _VP]),
+    "csa2_index_blocks": (ctypes.c_int, [ctypes.POINTER(CShape), _VP, _VP, _VP, _VP, _VP, _VP, _VP, _SZ, _VP]),
+    "csa2_index_tokens": (ctypes.c_int, [ctypes.POINTER(CShape), _VP, _VP, _VP, _VP, _VP, _VP, _VP, _VP, _VP,
+                                         _VP, _SZ, _VP]),
+    "csa2_topk": (ctypes.c_int, [ctypes.POINTER(CShape), _VP, _I32, _VP, _VP, _I32, _VP, _VP, _VP, _SZ, _VP]),
+    "csa2_sparse_attn": (ctypes.c_int, [ctypes.POINTER(CShape), _VP, _VP, _VP, _VP, _VP, _VP, _VP, _VP, _VP,
+                                        _VP, _SZ, _VP]),
+    "csa2_layer_group": (ctypes.c_int, [ctypes.POINTER(CShape), ctypes.POINTER(CLayer), _I32, _VP, _VP, _VP,
+                                        _VP, _VP, _VP, _VP, _SZ, _VP]),
+    "csa2_status_str": (ctypes.c_char_p, [ctypes.c_int]),
+    "csa2_read_device_error": (ctypes.c_int, [_VP, _VP, ctypes.POINTER(_I32)]),
+    "csa2_fast_path": (ctypes.c_int, [ctypes.POINTER(CShape), ctypes.POINTER(_I32), ctypes.POINTER(_I32)]),
+    "csa2_launch_count": (ctypes.c_ulonglong, []),
+}
+
+
+def lib() -> ctypes.CDLL:
+    """Load libcsa2.so (built in-tree); raise if it is missing."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(LIB_PATH):
+            raise RuntimeError(f"{LIB_PATH} is not built: run `python -m sparse_attention_decode_index_gb300.build` "
+                               "(or __graft_entry__.build()); the CSA2 path has no CPU fallback")
+        L = ctypes.CDLL(LIB_PATH)
+        for name, (res, args) in _SIGS.items():
+            fn = getattr(L, name)
+            fn.restype = res
+            fn.argtypes = args
+        _lib = L
+    return _lib
+
+
+def exported_symbols() -> Sequence[str]:
+    return list(_SIGS)
+
+
+def status_str(code: int) -> str:
+    try:
+        return lib().csa2_status_str(int(code)).decode()
+    except RuntimeError:
+        return STATUS.get(code, "unknown")
+
+
+# ------------------------------------------------------------------ marshalling helpers
+
+def c_shape(shape) -> CShape:
+    """Build the C shape from any object with the csa2_shape fields (e.g. workloads.Shape)."""
+    dt = getattr(shape, "dtype", "bf16")
+    dt = {"bf16": BF16, "f32": F32}.get(dt, dt)
+    return CShape(int(shape.batch), int(shape.n_entries), int(shape.idx_heads), int(shape.idx_dim),
+                  int(shape.block), int(shape.pool_blocks), int(shape.topk), int(shape.q_heads),
+                  int(shape.k_dim), int(shape.v_dim), int(shape.swa), float(getattr(shape, "scale", 0.0)),
+                  int(getattr(shape, "relu", 1)), int(dt))
+
+
+def elem_dtype(shape) -> torch.dtype:
+    return torch.float32 if getattr(shape, "dtype", "bf16") in ("f32", F32) else torch.bfloat16
+
+
+def _ptr(t: Optional[torch.Tensor], dtype: Optional[torch.dtype] = None, name: str = "tensor"):
+    if t is None:
+        return None
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a torch tensor")
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor (the library takes device pointers)")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if dtype is not None and t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+    return t.data_ptr()
+
+
+def _stream(stream) -> Optional[int]:
+    if stream is None:
+        return torch.cuda.current_stream().cuda_stream
+    return getattr(stream, "cuda_stream", stream)
+
+
+def _check(status: int, what: str):
+    if status != OK:
+        raise CSA2Error(status, what)
+
+
+# ------------------------------------------------------------------ entry points
+
+def workspace_bytes(shape) -> int:
+    s = c_shape(shape)
+    n = lib().csa2_workspace_bytes(ctypes.byref(s))
+    if n == 0:
+        raise CSA2Error(-1, "csa2_workspace_bytes")
+    return int(n)
+
+
+def workspace_init(ws: torch.Tensor, stream=None):
+    _check(lib().csa2_workspace_init(_ptr(ws, torch.uint8, "ws"), ws.numel(), _stream(stream)),
+           "csa2_workspace_init")
+
+
+def workspace(shape, device=None, stream=None) -> torch.Tensor:
+    """Allocate (with torch) and initialise a workspace for ``shape``."""
+    ws = torch.empty(workspace_bytes(shape), dtype=torch.uint8, device=device or "cuda")
+    workspace_init(ws, stream)
+    return ws
+
+
+def block_keys(shape, k_idx, n_valid, kb, ws, round_to_int: bool = True, stream=None):
+    s = c_shape(shape)
+    e = elem_dtype(shape)
+    _check(lib().csa2_block_keys(ctypes.byref(s), _ptr(k_idx, e, "k_idx"), _ptr(n_valid, torch.int32, "n_valid"),
+                                 int(bool(round_to_int)), _ptr(kb, e, "kb"), _ptr(ws, torch.uint8, "ws"),
+                                 ws.numel(), _stream(stream)), "csa2_block_keys")
+
+
+def index_blocks(shape, q_idx, w, kb, n_valid, pool_out, n_pool_out, ws, stream=None):
+    s = c_shape(shape)
+    e = elem_dtype(shape)
+    _check(lib().csa2_index_blocks(ctypes.byref(s), _ptr(q_idx, e, "q_idx"), _ptr(w, torch.float32, "w"),
+                                   _ptr(kb, e, "kb"), _ptr(n_valid, torch.int32, "n_valid"),
+                                   _ptr(pool_out, torch.int32, "pool_out"),
+                                   _ptr(n_pool_out, torch.int32, "n_pool_out"), _ptr(ws, torch.uint8, "ws"),
+                                   ws.numel(), _stream(stream)), "csa2_index_blocks")
+
+
+def index_tokens(shape, q_idx, w, k_idx, n_valid, scores_out, ws, pool=None, n_pool=None, cand_out=None,
+                 n_cand_out=None, stream=None):
+    s = c_shape(shape)
+    e = elem_dtype(shape)
+    _check(lib().csa2_index_tokens(ctypes.byref(s), _ptr(q_idx, e, "q_idx"), _ptr(w, torch.float32, "w"),
+                                   _ptr(k_idx, e, "k_idx"), _ptr(n_valid, torch.int32, "n_valid"),
+                                   _ptr(pool, torch.int32, "pool"), _ptr(n_pool, torch.int32, "n_pool"),
+                                   _ptr(scores_out, torch.float32, "scores_out"),
+                                   _ptr(cand_out, torch.int32, "cand_out"),
+                                   _ptr(n_cand_out, torch.int32, "n_cand_out"), _ptr(ws, torch.uint8, "ws"),
+                                   ws.numel(), _stream(stream)), "csa2_index_tokens")
+
+
+def topk(shape, scores, k: int, idx_out, ws, cand=None, n_cand=None, score_out=None, stream=None):
+    s = c_shape(shape)
+    ld = scores.shape[-1]
+    _check(lib().csa2_topk(ctypes.byref(s), _ptr(scores, torch.float32, "scores"), int(ld),
+                           _ptr(cand, torch.int32, "cand"), _ptr(n_cand, torch.int32, "n_cand"), int(k),
+                           _ptr(idx_out, torch.int32, "idx_out"), _ptr(score_out, torch.float32, "score_out"),
+                           _ptr(ws, torch.uint8, "ws"), ws.numel(), _stream(stream)), "csa2_topk")
+
+
+def sparse_attn(shape, q, k_main, v_main, idx, k_swa, v_swa, n_swa, out, ws, lse=None, stream=None):
+    s = c_shape(shape)
+    e = elem_dtype(shape)
+    _check(lib().csa2_sparse_attn(ctypes.byref(s), _ptr(q, e, "q"), _ptr(k_main, e, "k_main"),
+                                  _ptr(v_main, e, "v_main"), _ptr(idx, torch.int32, "idx"),
+                                  _ptr(k_swa, e, "k_swa"), _ptr(v_swa, e, "v_swa"),
+                                  _ptr(n_swa, torch.int32, "n_swa"), _ptr(out, torch.float32, "out"),
+                                  _ptr(lse, torch.float32, "lse"), _ptr(ws, torch.uint8, "ws"), ws.numel(),
+                                  _stream(stream)), "csa2_sparse_attn")
+
+
+def _layer(L, e) -> CLayer:
+    g = (lambda k: L.get(k)) if isinstance(L, dict) else (lambda k: getattr(L, k, None))
+    return CLayer(int(g("mode")), int(g("hier") or 0), _ptr(g("q"), e, "q"), _ptr(g("q_idx"), e, "q_idx"),
+                  _ptr(g("w_idx"), torch.float32, "w_idx"), _ptr(g("k_swa"), e, "k_swa"),
+                  _ptr(g("v_swa"), e, "v_swa"), _ptr(g("out"), torch.float32, "out"),
+                  _ptr(g("lse"), torch.float32, "lse"), _ptr(g("idx_out"), torch.int32, "idx_out"))
+
+
+class LayerGroupCall:
+    """A prepared csa2_layer_group call (marshalled once, launched many times)."""
+
+    def __init__(self, shape, layers: Iterable, k_main, v_main, k_idx, kb, n_valid, n_swa, ws):
+        e = elem_dtype(shape)
+        self._keep = (layers, k_main, v_main, k_idx, kb, n_valid, n_swa, ws)
+        self.shape = c_shape(shape)
+        ls = [_layer(L, e) for L in layers]
+        self.layers = (CLayer * len(ls))(*ls)
+        self.n = len(ls)
+        self.args = (_ptr(k_main, e, "k_main"), _ptr(v_main, e, "v_main"), _ptr(k_idx, e, "k_idx"),
+                     _ptr(kb, e, "kb"), _ptr(n_valid, torch.int32, "n_valid"), _ptr(n_swa, torch.int32, "n_swa"),
+                     _ptr(ws, torch.uint8, "ws"), ws.numel())
+
+    def __call__(self, stream=None):
+        _check(lib().csa2_layer_group(ctypes.byref(self.shape), self.layers, self.n, *self.args, _stream(stream)),
+               "csa2_layer_group")
+
+
+def layer_group(shape, layers, k_main, v_main, k_idx, kb, n_valid, n_swa, ws, stream=None):
+    LayerGroupCall(shape, layers, k_main, v_main, k_idx, kb, n_valid, n_swa, ws)(stream)
+
+
+def read_device_error(ws, stream=None):
+    """Synchronise and read/clear the sticky device error word: (status, detail bits)."""
+    d = _I32(0)
+    st = lib().csa2_read_device_error(_ptr(ws, torch.uint8, "ws"), _stream(stream), ctypes.byref(d))
+    return int(st), int(d.value)
+
+
+def launch_count() -> int:
+    """Kernel launches enqueued by the library so far (captured graph launches count once)."""
+    return int(lib().csa2_launch_count())
+
+
+def fast_path(shape):
+    s = c_shape(shape)
+    a, b = _I32(0), _I32(0)
+    lib().csa2_fast_path(ctypes.byref(s), ctypes.byref(a), ctypes.byref(b))
+    return bool(a.value), bool(b.value)
+
+
+# ------------------------------------------------------------------ workload upload
+
+def to_device_tensor(arr, device="cuda") -> torch.Tensor:
+    """numpy -> device tensor; uint16 arrays hold bf16 bit patterns."""
+    import numpy as np
+    a = np.ascontiguousarray(arr)
+    if a.dtype == np.uint16:
+        return torch.from_numpy(a.view(np.int16)).to(device).view(torch.bfloat16)
+    return torch.from_numpy(a).to(device)
+
+
+def upload(wl, device="cuda", with_outputs: bool = True):
+    """Copy a workloads.Workload to the device and allocate outputs / workspace.
+
+    Returns a dict with the group tensors, the per-layer dicts (accepted by
+    ``layer_group``) and a workspace.  Block summary keys are left to
+    ``block_keys`` (cache-side maintenance)."""
+    sh = wl.shape
+    d = dict(k_main=to_device_tensor(wl.k_main, device), v_main=to_device_tensor(wl.v_main, device),
+             k_idx=to_device_tensor(wl.k_idx, device),
+             n_valid=torch.from_numpy(wl.n_valid.astype("int32")).to(device),
+             n_swa=torch.from_numpy(wl.n_swa.astype("int32")).to(device))
+    nb = -(-sh.n_entries // sh.block)
+    d["kb"] = torch.zeros((sh.batch, nb, sh.idx_dim), dtype=elem_dtype(sh), device=device)
+    layers = []
+    for L in wl.layers:
+        y = dict(mode=L.mode, hier=L.hier, q=to_device_tensor(L.q, device), k_swa=to_device_tensor(L.k_swa, device),
+                 v_swa=to_device_tensor(L.v_swa, device))
+        if L.q_idx is not None:
+            y["q_idx"] = to_device_tensor(L.q_idx, device)
+            y["w_idx"] = to_device_tensor(L.w_idx, device)
+        if with_outputs:
+            y["out"] = torch.empty((sh.batch, sh.q_heads, sh.v_dim), dtype=torch.float32, device=device)
+            y["lse"] = torch.empty((sh.batch, sh.q_heads), dtype=torch.float32, device=device)
+            if L.mode != REUSE:
+                y["idx_out"] = torch.empty((sh.batch, sh.topk), dtype=torch.int32, device=device)
+        layers.append(y)
+    d["layers"] = layers
+    d["ws"] = workspace(sh, device)
+    return d

@@ -1,0 +1,339 @@
+// Sparse gather-attention: for every query head h
+//     o_h = softmax(scale * q_h [K_main[idx]; K_swa]^T) [V_main[idx]; V_swa]
+// one softmax over the selected main-KV rows plus the SWA rows
+// (DeepSeek V4.1 Flash architecture page, bullet "Sparse attention": each
+// query reads its Top-512 main-KV entries plus a 128-token SWA window; "CSA2
+// with cross-layer reuse": every mode computes its own main Q and SWA KV).
+//
+// Fast path (bf16, 64 heads sharing one KV head, dk 192, dv 128): the
+// 512 + 128 key slots of one query are split over a thread-block cluster of
+// ceil(slots / 128) CTAs.  Each CTA gathers its 128 K rows (384 B) and V rows
+// (256 B) plus the query (64 x 384 B) into padded shared-memory rows with one
+// bulk (TMA) copy per row, all completing on a single mbarrier; invalid slots
+// (index -1, or beyond n_swa) are zero-filled and masked.  Four warps each own
+// 16 heads: S = Q K^T and O = P V run on mma.sync m16n8k16 (bf16 in, fp32
+// accumulate), softmax in fp32 (base 2).  The partial (m, l, O) of every CTA
+// is merged in fixed CTA order through distributed shared memory, so no
+// partials touch global memory and the result is deterministic.
+#include "common.cuh"
+#include "internal.h"
+
+namespace csa2 {
+
+namespace {
+
+constexpr int kH = 64, kDk = 192, kDv = 128;
+constexpr int kSlots = 128;                       // key slots per CTA
+constexpr int kThreads = 128;
+constexpr int kKRow = kDk * 2 + 16;               // 400 B: padded so ldmatrix rows hit distinct banks
+constexpr int kVRow = kDv * 2 + 16;               // 272 B
+constexpr int kQRow = kKRow;
+constexpr int kORow = kDv + 4;                    // fp32 partial O row (floats)
+constexpr int kMaxCluster = 8;
+
+constexpr int kOffQ = 0;
+constexpr int kOffK = kOffQ + kH * kQRow;         // 25,600
+constexpr int kOffV = kOffK + kSlots * kKRow;     // 76,800
+constexpr int kOffM = kOffV + kSlots * kVRow;     // 111,616
+constexpr int kOffL = kOffM + kH * 4;
+constexpr int kOffValid = kOffL + kH * 4;
+constexpr int kOffBar = kOffValid + kSlots * 4;
+constexpr int kSmemBytes = kOffBar + 16;
+static_assert(kH * kORow * 4 <= kSlots * kKRow, "partial O must fit in the K region");
+
+__global__ void __launch_bounds__(kThreads) attn_mma_kernel(const AttnArgs a) {
+  extern __shared__ __align__(128) uint8_t smem[];
+  uint8_t* sQ = smem + kOffQ;
+  uint8_t* sK = smem + kOffK;
+  uint8_t* sV = smem + kOffV;
+  float* sM = reinterpret_cast<float*>(smem + kOffM);
+  float* sL = reinterpret_cast<float*>(smem + kOffL);
+  int* sValid = reinterpret_cast<int*>(smem + kOffValid);
+  uint64_t* bar = reinterpret_cast<uint64_t*>(smem + kOffBar);
+  float* sO = reinterpret_cast<float*>(smem + kOffK);   // reused after S = QK^T
+
+  const int b = blockIdx.y;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int g = lane >> 2, t = lane & 3;
+  const uint32_t crank = cluster_rank(), ncta = cluster_size();
+
+  if (tid == 0) {
+    mbar_init(bar, kThreads);
+    mbar_fence_init();
+  }
+  __syncthreads();
+
+  // --- gather: thread `tid` owns key slot (blockIdx.x * 128 + tid)
+  const int slot = blockIdx.x * kSlots + tid;
+  const uint8_t* ksrc = nullptr;
+  const uint8_t* vsrc = nullptr;
+  if (slot < a.topk) {
+    const int e = a.idx[(long long)b * a.topk + slot];
+    if (e >= a.n_entries) report(a.err, kErrBadIndex, e);
+    if (e >= 0 && e < a.n_entries) {
+      const long long r = (long long)b * a.n_entries + e;
+      ksrc = static_cast<const uint8_t*>(a.k_main) + r * (kDk * 2);
+      vsrc = static_cast<const uint8_t*>(a.v_main) + r * (kDv * 2);
+    }
+  } else if (slot < a.topk + a.swa) {
+    const int j = slot - a.topk;
+    const int ns = clamp_count(a.n_swa[b], a.swa, a.err);
+    if (j < ns) {
+      const long long r = (long long)b * a.swa + j;
+      ksrc = static_cast<const uint8_t*>(a.k_swa) + r * (kDk * 2);
+      vsrc = static_cast<const uint8_t*>(a.v_swa) + r * (kDv * 2);
+    }
+  }
+  const bool valid = ksrc != nullptr;
+  sValid[tid] = valid ? 1 : 0;
+  uint32_t tx = valid ? uint32_t(kDk * 2 + kDv * 2) : 0u;
+  if (tid < kH) tx += kDk * 2;
+  mbar_arrive_expect_tx(bar, tx);
+  if (valid) {
+    bulk_g2s(sK + tid * kKRow, ksrc, kDk * 2, bar);
+    bulk_g2s(sV + tid * kVRow, vsrc, kDv * 2, bar);
+  } else {
+    const uint4 z = make_uint4(0u, 0u, 0u, 0u);
+    for (int i = 0; i < kDk * 2; i += 16) *reinterpret_cast<uint4*>(sK + tid * kKRow + i) = z;
+    for (int i = 0; i < kDv * 2; i += 16) *reinterpret_cast<uint4*>(sV + tid * kVRow + i) = z;
+  }
+  if (tid < kH)
+    bulk_g2s(sQ + tid * kQRow, static_cast<const uint8_t*>(a.q) + ((long long)b * kH + tid) * (kDk * 2),
+             kDk * 2, bar);
+  const bool ok = mbar_wait(bar, 0);
+  if (!ok) {
+    // record the stall, give the copies in flight one more bounded wait
+    report(a.err, kErrTimeout, slot);
+    mbar_wait(bar, 0);
+  }
+  __syncthreads();
+
+  // --- S = Q K^T for heads [16w, 16w + 16) x 128 keys
+  float s[16][4];
+#pragma unroll
+  for (int j = 0; j < 16; ++j) s[j][0] = s[j][1] = s[j][2] = s[j][3] = 0.f;
+  const uint8_t* qrow = sQ + (warp * 16 + (lane & 15)) * kQRow + (lane >> 4) * 16;
+  const uint8_t* krow = sK + ((lane & 7) + 8 * (lane >> 4)) * kKRow + ((lane >> 3) & 1) * 16;
+#pragma unroll 2
+  for (int ks = 0; ks < kDk / 16; ++ks) {
+    uint32_t a0, a1, a2, a3;
+    ldsm_x4(a0, a1, a2, a3, qrow + ks * 32);
+#pragma unroll
+    for (int jp = 0; jp < 8; ++jp) {
+      uint32_t b0, b1, b2, b3;
+      ldsm_x4(b0, b1, b2, b3, krow + jp * 16 * kKRow + ks * 32);
+      mma_bf16(s[2 * jp], a0, a1, a2, a3, b0, b1);
+      mma_bf16(s[2 * jp + 1], a0, a1, a2, a3, b2, b3);
+    }
+  }
+
+  // --- softmax (base 2): rows g and g + 8 of this warp's 16 heads
+  const float sl2 = a.scale * 1.4426950408889634f;
+  float m0 = -INFINITY, m1 = -INFINITY;
+#pragma unroll
+  for (int j = 0; j < 16; ++j) {
+    const bool v0 = sValid[8 * j + 2 * t] != 0, v1 = sValid[8 * j + 2 * t + 1] != 0;
+    s[j][0] = v0 ? s[j][0] * sl2 : -INFINITY;
+    s[j][1] = v1 ? s[j][1] * sl2 : -INFINITY;
+    s[j][2] = v0 ? s[j][2] * sl2 : -INFINITY;
+    s[j][3] = v1 ? s[j][3] * sl2 : -INFINITY;
+    m0 = fmaxf(m0, fmaxf(s[j][0], s[j][1]));
+    m1 = fmaxf(m1, fmaxf(s[j][2], s[j][3]));
+  }
+  m0 = fmaxf(m0, __shfl_xor_sync(0xffffffffu, m0, 1));
+  m0 = fmaxf(m0, __shfl_xor_sync(0xffffffffu, m0, 2));
+  m1 = fmaxf(m1, __shfl_xor_sync(0xffffffffu, m1, 1));
+  m1 = fmaxf(m1, __shfl_xor_sync(0xffffffffu, m1, 2));
+  const float b0s = m0 == -INFINITY ? 0.f : m0;
+  const float b1s = m1 == -INFINITY ? 0.f : m1;
+  float l0 = 0.f, l1 = 0.f;
+#pragma unroll
+  for (int j = 0; j < 16; ++j) {
+    s[j][0] = exp2f(s[j][0] - b0s);
+    s[j][1] = exp2f(s[j][1] - b0s);
+    s[j][2] = exp2f(s[j][2] - b1s);
+    s[j][3] = exp2f(s[j][3] - b1s);
+    l0 += s[j][0] + s[j][1];
+    l1 += s[j][2] + s[j][3];
+  }
+  l0 += __shfl_xor_sync(0xffffffffu, l0, 1);
+  l0 += __shfl_xor_sync(0xffffffffu, l0, 2);
+  l1 += __shfl_xor_sync(0xffffffffu, l1, 1);
+  l1 += __shfl_xor_sync(0xffffffffu, l1, 2);
+
+  // --- O = P V (P from the S accumulators, V rows via ldmatrix.trans)
+  float o[16][4];
+#pragma unroll
+  for (int j = 0; j < 16; ++j) o[j][0] = o[j][1] = o[j][2] = o[j][3] = 0.f;
+  const uint8_t* vrow = sV + ((lane & 7) + 8 * ((lane >> 3) & 1)) * kVRow + (lane >> 4) * 16;
+#pragma unroll
+  for (int kk = 0; kk < kSlots / 16; ++kk) {
+    const uint32_t p0 = pack_bf16(s[2 * kk][0], s[2 * kk][1]);
+    const uint32_t p1 = pack_bf16(s[2 * kk][2], s[2 * kk][3]);
+    const uint32_t p2 = pack_bf16(s[2 * kk + 1][0], s[2 * kk + 1][1]);
+    const uint32_t p3 = pack_bf16(s[2 * kk + 1][2], s[2 * kk + 1][3]);
+#pragma unroll
+    for (int dp = 0; dp < kDv / 16; ++dp) {
+      uint32_t b0, b1, b2, b3;
+      ldsm_x4_t(b0, b1, b2, b3, vrow + kk * 16 * kVRow + dp * 32);
+      mma_bf16(o[2 * dp], p0, p1, p2, p3, b0, b1);
+      mma_bf16(o[2 * dp + 1], p0, p1, p2, p3, b2, b3);
+    }
+  }
+
+  // --- partial (m, l, O) of this CTA into shared memory (O over the K region)
+  __syncthreads();
+  const int h0 = warp * 16 + g, h1 = h0 + 8;
+#pragma unroll
+  for (int j = 0; j < 16; ++j) {
+    *reinterpret_cast<float2*>(sO + h0 * kORow + 8 * j + 2 * t) = make_float2(o[j][0], o[j][1]);
+    *reinterpret_cast<float2*>(sO + h1 * kORow + 8 * j + 2 * t) = make_float2(o[j][2], o[j][3]);
+  }
+  if (t == 0) {
+    sM[h0] = m0;
+    sL[h0] = l0;
+    sM[h1] = m1;
+    sL[h1] = l1;
+  }
+  cluster_sync_all();
+
+  // --- merge the cluster's partials in CTA order; thread owns (head, dim) pairs
+  const int nthreads = int(ncta) * kThreads;
+  for (int e = int(crank) * kThreads + tid; e < kH * kDv; e += nthreads) {
+    const int h = e / kDv, d = e % kDv;
+    float mr[kMaxCluster];
+    float M = -INFINITY;
+    for (uint32_t r = 0; r < ncta; ++r) {
+      mr[r] = dsmem_ld_f32(dsmem_addr(sM + h, r));
+      M = fmaxf(M, mr[r]);
+    }
+    float L = 0.f, O = 0.f;
+    if (M != -INFINITY) {
+      for (uint32_t r = 0; r < ncta; ++r) {
+        if (mr[r] == -INFINITY) continue;
+        const float f = exp2f(mr[r] - M);
+        L += f * dsmem_ld_f32(dsmem_addr(sL + h, r));
+        O += f * dsmem_ld_f32(dsmem_addr(sO + h * kORow + d, r));
+      }
+    }
+    const long long oi = ((long long)b * kH + h) * kDv + d;
+    a.out[oi] = M == -INFINITY ? 0.f : O / L;
+    if (d == 0 && a.lse != nullptr)
+      a.lse[(long long)b * kH + h] = M == -INFINITY ? -INFINITY : (M + log2f(L)) * 0.6931471805599453f;
+  }
+  cluster_sync_all();
+}
+
+// Generic path: any head count / dims / element type; one CTA per (query, head).
+__global__ void __launch_bounds__(128) attn_generic_kernel(const AttnArgs a) {
+  extern __shared__ float sh[];
+  const int b = blockIdx.y, h = blockIdx.x, tid = threadIdx.x;
+  const int nslots = a.topk + a.swa;
+  float* sq = sh;                       // [k_dim]
+  float* sp = sh + a.k_dim;             // [nslots] logits -> probabilities
+  float* red = sp + nslots;             // [32]
+  for (int i = tid; i < a.k_dim; i += blockDim.x)
+    sq[i] = load_elem(a.q, ((long long)b * a.heads + h) * a.k_dim + i, a.dtype);
+  __syncthreads();
+  const int ns = clamp_count(a.n_swa[b], a.swa, a.err);
+  float mx = -INFINITY;
+  for (int j = tid; j < nslots; j += blockDim.x) {
+    const void* kb = nullptr;
+    long long r = 0;
+    if (j < a.topk) {
+      const int e = a.idx[(long long)b * a.topk + j];
+      if (e >= a.n_entries && h == 0) report(a.err, kErrBadIndex, e);
+      if (e >= 0 && e < a.n_entries) {
+        kb = a.k_main;
+        r = (long long)b * a.n_entries + e;
+      }
+    } else if (j - a.topk < ns) {
+      kb = a.k_swa;
+      r = (long long)b * a.swa + (j - a.topk);
+    }
+    float v = -INFINITY;
+    if (kb != nullptr) {
+      float d = 0.f;
+      for (int i = 0; i < a.k_dim; ++i) d = __fmaf_rn(sq[i], load_elem(kb, r * a.k_dim + i, a.dtype), d);
+      v = d * a.scale;
+    }
+    sp[j] = v;
+    mx = fmaxf(mx, v);
+  }
+  for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+  if ((tid & 31) == 0) red[tid >> 5] = mx;
+  __syncthreads();
+  mx = red[0];
+  for (int w = 1; w < int(blockDim.x >> 5); ++w) mx = fmaxf(mx, red[w]);
+  __syncthreads();
+  float sum = 0.f;
+  for (int j = tid; j < nslots; j += blockDim.x) {
+    const float p = mx == -INFINITY ? 0.f : expf(sp[j] - mx);
+    sp[j] = p;
+    sum += p;
+  }
+  for (int o = 16; o > 0; o >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
+  if ((tid & 31) == 0) red[tid >> 5] = sum;
+  __syncthreads();
+  sum = 0.f;
+  for (int w = 0; w < int(blockDim.x >> 5); ++w) sum += red[w];
+  for (int d = tid; d < a.v_dim; d += blockDim.x) {
+    float acc = 0.f;
+    for (int j = 0; j < nslots; ++j) {
+      const float p = sp[j];
+      if (p == 0.f) continue;
+      long long r;
+      const void* vb;
+      if (j < a.topk) {
+        vb = a.v_main;
+        r = (long long)b * a.n_entries + a.idx[(long long)b * a.topk + j];
+      } else {
+        vb = a.v_swa;
+        r = (long long)b * a.swa + (j - a.topk);
+      }
+      acc = __fmaf_rn(p, load_elem(vb, r * a.v_dim + d, a.dtype), acc);
+    }
+    a.out[((long long)b * a.heads + h) * a.v_dim + d] = mx == -INFINITY ? 0.f : acc / sum;
+  }
+  if (tid == 0 && a.lse != nullptr)
+    a.lse[(long long)b * a.heads + h] = mx == -INFINITY ? -INFINITY : mx + logf(sum);
+}
+
+}  // namespace
+
+cudaError_t launch_attn(const AttnArgs& a, bool fast, int batch, cudaStream_t st) {
+  if (batch == 0) return cudaSuccess;
+  if (!fast) {
+    const size_t smem = (size_t(a.k_dim) + a.topk + a.swa + 32) * sizeof(float);
+    dim3 grid(unsigned(a.heads), unsigned(batch));
+    note_launch();
+    attn_generic_kernel<<<grid, 128, smem, st>>>(a);
+    return cudaGetLastError();
+  }
+  static bool attr_set = false;
+  if (!attr_set) {
+    cudaError_t e = cudaFuncSetAttribute(attn_mma_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+    if (e != cudaSuccess) return e;
+    attr_set = true;
+  }
+  const int ncta = (a.topk + a.swa + kSlots - 1) / kSlots;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(unsigned(ncta), unsigned(batch), 1);
+  cfg.blockDim = dim3(kThreads, 1, 1);
+  cfg.dynamicSmemBytes = kSmemBytes;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = unsigned(ncta);
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  note_launch();
+  return cudaLaunchKernelEx(&cfg, attn_mma_kernel, a);
+}
+
+int attn_max_cluster() { return kMaxCluster; }
+int attn_slots_per_cta() { return kSlots; }
+
+}  // namespace csa2

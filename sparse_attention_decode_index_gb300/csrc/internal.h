@@ -1,0 +1,93 @@
+// Internal interface between the C-ABI host code (api.cu) and the kernel
+// translation units.  Not installed; not part of the public ABI.
+#pragma once
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace csa2 {
+
+// Bits of the sticky device error word (word 0 of the workspace header).
+constexpr int kErrBadIndex = 1;   // a main-KV index outside [0, n_entries)
+constexpr int kErrBadCount = 2;   // n_valid / n_swa / n_pool / n_cand outside its range
+constexpr int kErrTimeout = 4;    // a bounded wait on an mbarrier gave up
+constexpr int kErrBadPool = 8;    // a pooled block id outside [0, ceil(n_valid / block))
+
+// Indexer scoring: s = sum_h w_h * ReLU(q_h . k) over a flat row range or the
+// entries of pooled blocks.
+struct IndexerArgs {
+  const void* keys;          // [B, rows_per_seq, dim] (indexer keys or block keys)
+  long long rows_per_seq;    // row capacity per sequence
+  const void* q_idx;         // [B, heads, dim]
+  const float* w;            // [B, heads]
+  const int* n_valid;        // [B] valid compressed entries per query
+  int valid_cap;             // capacity n_valid is checked against
+  int div;                   // flat: valid rows = ceil(n_valid / div) (1 or block)
+  const int* pool;           // pooled: [B, pool_cap] ascending block ids
+  const int* n_pool;         // pooled: [B]
+  int pool_cap;              // pooled: row stride of `pool`
+  int block;                 // entries per block
+  float* scores;             // [B, ld]
+  int* cand;                 // [B, ld] candidate entry ids (nullable when flat)
+  int* n_cand;               // [B] candidate positions written (nullable)
+  long long ld;              // row stride of scores / cand
+  int per_cta;               // flat: rows per CTA; pooled: pool positions per CTA
+  int relu;
+  int heads, dim, dtype;     // generic kernel only
+  int* err;                  // device error word (nullable)
+};
+
+struct TopkArgs {
+  const float* scores;       // row r = b * rows_per_b ... ; element (r, pos)
+  long long ld_in;           // row stride of scores / cand
+  const int* cand;           // nullable: id = position; entries < 0 are skipped
+  const int* n_cand;         // [B] positions to consider (nullable -> n_fixed)
+  int n_fixed;
+  int n_cap;                 // n_cand is clamped to this
+  int chunk;                 // positions per CTA (grid.x = chunks)
+  int k;
+  int* idx_out;              // [B, chunks, k]
+  float* score_out;          // [B, chunks, k] (nullable)
+  int* n_out;                // [B] number selected (nullable; single-chunk launches only)
+  int* err;
+};
+
+struct AttnArgs {
+  const void* q;             // [B, H, dk]
+  const void* k_main;        // [B, N, dk]
+  const void* v_main;        // [B, N, dv]
+  const int* idx;            // [B, topk]
+  const void* k_swa;         // [B, W, dk]
+  const void* v_swa;         // [B, W, dv]
+  const int* n_swa;          // [B]
+  float* out;                // [B, H, dv]
+  float* lse;                // [B, H] (nullable)
+  int n_entries, topk, swa;
+  int heads, k_dim, v_dim, dtype;
+  float scale;               // softmax scale (natural-log domain)
+  int* err;
+};
+
+struct BlockKeyArgs {
+  const void* k_idx;         // [B, N, dim]
+  const int* n_valid;        // [B]
+  void* kb;                  // [B, NB, dim]
+  int n_entries, nb_cap, dim, block, round_to_int, dtype;
+  int* err;
+};
+
+int device_sm_count();
+// Counts kernel launches enqueued by the library (diagnostics: csa2_launch_count).
+void note_launch();
+
+cudaError_t launch_block_keys(const BlockKeyArgs& a, int batch, cudaStream_t st);
+// fast: bf16, 8 heads x 64 dims, block 8 (pooled)
+cudaError_t launch_indexer(const IndexerArgs& a, bool pooled, bool fast, int batch, int max_rows,
+                           cudaStream_t st);
+cudaError_t launch_topk(const TopkArgs& a, int chunks, int batch, cudaStream_t st);
+int topk_max_chunk();
+int attn_max_cluster();
+int attn_slots_per_cta();
+// fast: bf16, 64 heads, dk 192, dv 128
+cudaError_t launch_attn(const AttnArgs& a, bool fast, int batch, cudaStream_t st);
+
+}  // namespace csa2

@@ -37,6 +37,8 @@ fp32 integers uniform on {1,2,3}.
 from __future__ import annotations
 
 import dataclasses
+import os
+from concurrent.futures import ThreadPoolExecutor
 from typing import List, Optional
 
 import numpy as np
@@ -103,16 +105,48 @@ def _rng(*key: int) -> np.random.Generator:
     return np.random.default_rng(np.random.SeedSequence([int(k) for k in key]))
 
 
-def _normal_bf16(rng, shape, div):
-    x = rng.standard_normal(size=shape, dtype=np.float32)
-    if div != 1.0:
-        x *= np.float32(1.0 / div)
-    return f32_to_bf16_bits(x)
+_CHUNK = 1 << 21                     # values per independently seeded chunk
+_THREADS = max(1, min(16, os.cpu_count() or 1))
+_INT_BF16 = None
 
 
-def _int_bf16(rng, shape, lo=-4, hi=4):
-    x = rng.integers(lo, hi + 1, size=shape, dtype=np.int32).astype(np.float32)
-    return f32_to_bf16_bits(x)
+def _int_table():
+    global _INT_BF16
+    if _INT_BF16 is None:
+        _INT_BF16 = f32_to_bf16_bits(np.arange(-4, 5, dtype=np.float32))
+    return _INT_BF16
+
+
+def _draw(shape, key, kind: str, div: float = 1.0, bf16: bool = True) -> np.ndarray:
+    """Draw a tensor in fixed chunks, chunk c from the stream (*key, c).
+
+    ``kind``: "normal" (N(0,1)/div) or "int" (uniform integers on {-4..4}).
+    The result does not depend on the number of threads used.
+    """
+    n = int(np.prod(shape))
+    out = np.empty(n, dtype=np.uint16 if bf16 else np.float32)
+    scale = np.float32(1.0 / div)
+
+    def work(c):
+        lo, hi = c * _CHUNK, min(n, (c + 1) * _CHUNK)
+        rng = _rng(*key, c)
+        if kind == "int":
+            code = rng.integers(0, 9, size=hi - lo, dtype=np.int8)
+            out[lo:hi] = _int_table()[code] if bf16 else (code.astype(np.float32) - 4)
+            return
+        x = rng.standard_normal(size=hi - lo, dtype=np.float32)
+        if div != 1.0:
+            x *= scale
+        out[lo:hi] = f32_to_bf16_bits(x) if bf16 else x
+
+    chunks = range(-(-n // _CHUNK))
+    if len(chunks) > 1 and _THREADS > 1:
+        with ThreadPoolExecutor(_THREADS) as ex:
+            list(ex.map(work, chunks))
+    else:
+        for c in chunks:
+            work(c)
+    return out.reshape(shape)
 
 
 def _weights(rng, shape):
@@ -144,37 +178,32 @@ def make_workload(shape: Shape, modes: List[int], *, seed: int = 0, cfg_id: int 
     B, N = shape.batch, shape.n_entries
     f32 = shape.dtype == "f32"
 
-    def kv(rng, shp, d):
-        if f32:
-            return rng.standard_normal(size=shp, dtype=np.float32)
-        return _normal_bf16(rng, shp, float(np.sqrt(d)))
+    def kv(key, shp, d):
+        return _draw(shp, key, "normal", 1.0 if f32 else float(np.sqrt(d)), bf16=not f32)
 
-    def q_of(rng, shp):
-        if f32:
-            return rng.standard_normal(size=shp, dtype=np.float32)
-        return _normal_bf16(rng, shp, 1.0)
+    def q_of(key, shp):
+        return _draw(shp, key, "normal", 1.0, bf16=not f32)
 
-    def idxv(rng, shp):
+    def idxv(key, shp):
         if f32 or not int_indexer:
-            x = rng.standard_normal(size=shp, dtype=np.float32)
-            return x if f32 else f32_to_bf16_bits(x)
-        return _int_bf16(rng, shp)
+            return _draw(shp, key, "normal", 1.0, bf16=not f32)
+        return _draw(shp, key, "int")
 
-    k_main = kv(_rng(seed, cfg_id, 1), (B, N, shape.k_dim), shape.k_dim)
-    v_main = kv(_rng(seed, cfg_id, 2), (B, N, shape.v_dim), shape.v_dim)
-    k_idx = idxv(_rng(seed, cfg_id, 3), (B, N, shape.idx_dim))
+    k_main = kv((seed, cfg_id, 1), (B, N, shape.k_dim), shape.k_dim)
+    v_main = kv((seed, cfg_id, 2), (B, N, shape.v_dim), shape.v_dim)
+    k_idx = idxv((seed, cfg_id, 3), (B, N, shape.idx_dim))
     if n_valid is None:
         n_valid = np.full(B, N, dtype=np.int32)
     if n_swa is None:
         n_swa = np.full(B, shape.swa, dtype=np.int32)
     layers = []
     for l, mode in enumerate(modes):
-        q = q_of(_rng(seed, cfg_id, 10, l), (B, shape.q_heads, shape.k_dim))
-        k_swa = kv(_rng(seed, cfg_id, 11, l), (B, shape.swa, shape.k_dim), shape.k_dim)
-        v_swa = kv(_rng(seed, cfg_id, 12, l), (B, shape.swa, shape.v_dim), shape.v_dim)
+        q = q_of((seed, cfg_id, 10, l), (B, shape.q_heads, shape.k_dim))
+        k_swa = kv((seed, cfg_id, 11, l), (B, shape.swa, shape.k_dim), shape.k_dim)
+        v_swa = kv((seed, cfg_id, 12, l), (B, shape.swa, shape.v_dim), shape.v_dim)
         q_idx = w = None
         if mode != REUSE:
-            q_idx = idxv(_rng(seed, cfg_id, 13, l), (B, shape.idx_heads, shape.idx_dim))
+            q_idx = idxv((seed, cfg_id, 13, l), (B, shape.idx_heads, shape.idx_dim))
             if f32:
                 w = np.ones((B, shape.idx_heads), dtype=np.float32)
             else:
