@@ -7,14 +7,18 @@
 //
 // Fast path (bf16, 64 heads sharing one KV head, dk 192, dv 128): the
 // 512 + 128 key slots of one query are split over a thread-block cluster of
-// ceil(slots / 128) CTAs.  Each CTA gathers its 128 K rows (384 B) and V rows
-// (256 B) plus the query (64 x 384 B) into padded shared-memory rows with one
-// bulk (TMA) copy per row, all completing on a single mbarrier; invalid slots
-// (index -1, or beyond n_swa) are zero-filled and masked.  Four warps each own
-// 16 heads: S = Q K^T and O = P V run on mma.sync m16n8k16 (bf16 in, fp32
-// accumulate), softmax in fp32 (base 2).  The partial (m, l, O) of every CTA
-// is merged in fixed CTA order through distributed shared memory, so no
-// partials touch global memory and the result is deterministic.
+// ceil(slots / 160) CTAs (4 for the architecture's 640 slots), sized so that two
+// CTAs fit per SM and every cluster of a 64-query batch is resident in one wave.
+// Each CTA gathers its 160 K rows (384 B) and V rows (256 B) into padded
+// shared-memory rows with one bulk (TMA) copy per row, all completing on one
+// mbarrier; invalid slots (index -1, or beyond n_swa) are zero-filled and
+// masked.  Four warps each own 16 heads; their Q fragments are loaded straight
+// into registers while the gather is in flight.  S = Q K^T and O = P V run on
+// mma.sync m16n8k16 (bf16 in, fp32 accumulate) with a base-2 fp32 softmax.
+// The partial (m, l, O) of every CTA is merged in fixed CTA order through
+// distributed shared memory: per-head factors exp2(m_c - M) / L first, then
+// 16-byte remote loads of the partial O rows.  No partial touches global
+// memory and the result is deterministic.
 #include "common.cuh"
 #include "internal.h"
 
@@ -23,31 +27,39 @@ namespace csa2 {
 namespace {
 
 constexpr int kH = 64, kDk = 192, kDv = 128;
-constexpr int kSlots = 128;                       // key slots per CTA
+constexpr int kSlots = 160;                       // key slots per CTA
+constexpr int kNT = kSlots / 8;                   // S n-tiles (8 keys each)
 constexpr int kThreads = 128;
 constexpr int kKRow = kDk * 2 + 16;               // 400 B: padded so ldmatrix rows hit distinct banks
 constexpr int kVRow = kDv * 2 + 16;               // 272 B
-constexpr int kQRow = kKRow;
-constexpr int kORow = kDv + 4;                    // fp32 partial O row (floats)
+constexpr int kORow = kDv + 4;                    // fp32 partial O row (floats), 16 B multiple
 constexpr int kMaxCluster = 8;
 
-constexpr int kOffQ = 0;
-constexpr int kOffK = kOffQ + kH * kQRow;         // 25,600
-constexpr int kOffV = kOffK + kSlots * kKRow;     // 76,800
-constexpr int kOffM = kOffV + kSlots * kVRow;     // 111,616
+constexpr int kOffK = 0;
+constexpr int kOffV = kOffK + kSlots * kKRow;     // 64,000
+constexpr int kOffM = kOffV + kSlots * kVRow;     // 107,520
 constexpr int kOffL = kOffM + kH * 4;
-constexpr int kOffValid = kOffL + kH * 4;
+constexpr int kOffF = kOffL + kH * 4;             // [kMaxCluster][kH] merge factors
+constexpr int kOffValid = kOffF + kMaxCluster * kH * 4;
 constexpr int kOffBar = kOffValid + kSlots * 4;
 constexpr int kSmemBytes = kOffBar + 16;
 static_assert(kH * kORow * 4 <= kSlots * kKRow, "partial O must fit in the K region");
+static_assert(kSlots % 16 == 0, "PV k-steps need 16-key groups");
 
-__global__ void __launch_bounds__(kThreads) attn_mma_kernel(const AttnArgs a) {
+CSA2_DEV void dsmem_ld_v4(float4& v, uint32_t addr) {
+  asm volatile("ld.shared::cluster.v4.f32 {%0,%1,%2,%3}, [%4];"
+               : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
+               : "r"(addr)
+               : "memory");
+}
+
+__global__ void __launch_bounds__(kThreads, 2) attn_mma_kernel(const AttnArgs a) {
   extern __shared__ __align__(128) uint8_t smem[];
-  uint8_t* sQ = smem + kOffQ;
   uint8_t* sK = smem + kOffK;
   uint8_t* sV = smem + kOffV;
   float* sM = reinterpret_cast<float*>(smem + kOffM);
   float* sL = reinterpret_cast<float*>(smem + kOffL);
+  float* sF = reinterpret_cast<float*>(smem + kOffF);
   int* sValid = reinterpret_cast<int*>(smem + kOffValid);
   uint64_t* bar = reinterpret_cast<uint64_t*>(smem + kOffBar);
   float* sO = reinterpret_cast<float*>(smem + kOffK);   // reused after S = QK^T
@@ -63,67 +75,82 @@ __global__ void __launch_bounds__(kThreads) attn_mma_kernel(const AttnArgs a) {
   }
   __syncthreads();
 
-  // --- gather: thread `tid` owns key slot (blockIdx.x * 128 + tid)
-  const int slot = blockIdx.x * kSlots + tid;
-  const uint8_t* ksrc = nullptr;
-  const uint8_t* vsrc = nullptr;
-  if (slot < a.topk) {
-    const int e = a.idx[(long long)b * a.topk + slot];
-    if (e >= a.n_entries) report(a.err, kErrBadIndex, e);
-    if (e >= 0 && e < a.n_entries) {
-      const long long r = (long long)b * a.n_entries + e;
-      ksrc = static_cast<const uint8_t*>(a.k_main) + r * (kDk * 2);
-      vsrc = static_cast<const uint8_t*>(a.v_main) + r * (kDv * 2);
+  // --- gather: thread `tid` owns key slots tid and tid + 128 of this CTA
+  uint32_t tx = 0;
+  const uint8_t* ksrc[2] = {nullptr, nullptr};
+  const uint8_t* vsrc[2] = {nullptr, nullptr};
+  const int ns = clamp_count(a.n_swa[b], a.swa, a.err);
+#pragma unroll
+  for (int j = 0; j < 2; ++j) {
+    const int ls = tid + j * kThreads;
+    if (ls >= kSlots) break;
+    const int slot = blockIdx.x * kSlots + ls;
+    if (slot < a.topk) {
+      const int e = a.idx[(long long)b * a.topk + slot];
+      if (e >= a.n_entries) report(a.err, kErrBadIndex, e);
+      if (e >= 0 && e < a.n_entries) {
+        const long long r = (long long)b * a.n_entries + e;
+        ksrc[j] = static_cast<const uint8_t*>(a.k_main) + r * (kDk * 2);
+        vsrc[j] = static_cast<const uint8_t*>(a.v_main) + r * (kDv * 2);
+      }
+    } else if (slot < a.topk + a.swa && slot - a.topk < ns) {
+      const long long r = (long long)b * a.swa + (slot - a.topk);
+      ksrc[j] = static_cast<const uint8_t*>(a.k_swa) + r * (kDk * 2);
+      vsrc[j] = static_cast<const uint8_t*>(a.v_swa) + r * (kDv * 2);
     }
-  } else if (slot < a.topk + a.swa) {
-    const int j = slot - a.topk;
-    const int ns = clamp_count(a.n_swa[b], a.swa, a.err);
-    if (j < ns) {
-      const long long r = (long long)b * a.swa + j;
-      ksrc = static_cast<const uint8_t*>(a.k_swa) + r * (kDk * 2);
-      vsrc = static_cast<const uint8_t*>(a.v_swa) + r * (kDv * 2);
-    }
+    sValid[ls] = ksrc[j] != nullptr ? 1 : 0;
+    if (ksrc[j] != nullptr) tx += kDk * 2 + kDv * 2;
   }
-  const bool valid = ksrc != nullptr;
-  sValid[tid] = valid ? 1 : 0;
-  uint32_t tx = valid ? uint32_t(kDk * 2 + kDv * 2) : 0u;
-  if (tid < kH) tx += kDk * 2;
   mbar_arrive_expect_tx(bar, tx);
-  if (valid) {
-    bulk_g2s(sK + tid * kKRow, ksrc, kDk * 2, bar);
-    bulk_g2s(sV + tid * kVRow, vsrc, kDv * 2, bar);
-  } else {
-    const uint4 z = make_uint4(0u, 0u, 0u, 0u);
-    for (int i = 0; i < kDk * 2; i += 16) *reinterpret_cast<uint4*>(sK + tid * kKRow + i) = z;
-    for (int i = 0; i < kDv * 2; i += 16) *reinterpret_cast<uint4*>(sV + tid * kVRow + i) = z;
+#pragma unroll
+  for (int j = 0; j < 2; ++j) {
+    const int ls = tid + j * kThreads;
+    if (ls >= kSlots) break;
+    if (ksrc[j] != nullptr) {
+      bulk_g2s(sK + ls * kKRow, ksrc[j], kDk * 2, bar);
+      bulk_g2s(sV + ls * kVRow, vsrc[j], kDv * 2, bar);
+    } else {
+      const uint4 z = make_uint4(0u, 0u, 0u, 0u);
+      for (int i = 0; i < kDk * 2; i += 16) *reinterpret_cast<uint4*>(sK + ls * kKRow + i) = z;
+      for (int i = 0; i < kDv * 2; i += 16) *reinterpret_cast<uint4*>(sV + ls * kVRow + i) = z;
+    }
   }
-  if (tid < kH)
-    bulk_g2s(sQ + tid * kQRow, static_cast<const uint8_t*>(a.q) + ((long long)b * kH + tid) * (kDk * 2),
-             kDk * 2, bar);
+
+  // --- Q A-fragments for heads 16w + g and 16w + g + 8, straight from global
+  uint32_t qa[kDk / 16][4];
+  {
+    const uint32_t* q0 = reinterpret_cast<const uint32_t*>(static_cast<const uint8_t*>(a.q) +
+                                                           ((long long)b * kH + warp * 16 + g) * (kDk * 2)) + t;
+    const uint32_t* q1 = q0 + 8 * (kDk / 2);
+#pragma unroll
+    for (int ks = 0; ks < kDk / 16; ++ks) {
+      qa[ks][0] = __ldg(q0 + ks * 8);
+      qa[ks][1] = __ldg(q1 + ks * 8);
+      qa[ks][2] = __ldg(q0 + ks * 8 + 4);
+      qa[ks][3] = __ldg(q1 + ks * 8 + 4);
+    }
+  }
   const bool ok = mbar_wait(bar, 0);
   if (!ok) {
     // record the stall, give the copies in flight one more bounded wait
-    report(a.err, kErrTimeout, slot);
+    report(a.err, kErrTimeout, b);
     mbar_wait(bar, 0);
   }
   __syncthreads();
 
-  // --- S = Q K^T for heads [16w, 16w + 16) x 128 keys
-  float s[16][4];
+  // --- S = Q K^T for heads [16w, 16w + 16) x 160 keys
+  float s[kNT][4];
 #pragma unroll
-  for (int j = 0; j < 16; ++j) s[j][0] = s[j][1] = s[j][2] = s[j][3] = 0.f;
-  const uint8_t* qrow = sQ + (warp * 16 + (lane & 15)) * kQRow + (lane >> 4) * 16;
+  for (int j = 0; j < kNT; ++j) s[j][0] = s[j][1] = s[j][2] = s[j][3] = 0.f;
   const uint8_t* krow = sK + ((lane & 7) + 8 * (lane >> 4)) * kKRow + ((lane >> 3) & 1) * 16;
-#pragma unroll 2
-  for (int ks = 0; ks < kDk / 16; ++ks) {
-    uint32_t a0, a1, a2, a3;
-    ldsm_x4(a0, a1, a2, a3, qrow + ks * 32);
 #pragma unroll
-    for (int jp = 0; jp < 8; ++jp) {
+  for (int ks = 0; ks < kDk / 16; ++ks) {
+#pragma unroll
+    for (int jp = 0; jp < kNT / 2; ++jp) {
       uint32_t b0, b1, b2, b3;
       ldsm_x4(b0, b1, b2, b3, krow + jp * 16 * kKRow + ks * 32);
-      mma_bf16(s[2 * jp], a0, a1, a2, a3, b0, b1);
-      mma_bf16(s[2 * jp + 1], a0, a1, a2, a3, b2, b3);
+      mma_bf16(s[2 * jp], qa[ks][0], qa[ks][1], qa[ks][2], qa[ks][3], b0, b1);
+      mma_bf16(s[2 * jp + 1], qa[ks][0], qa[ks][1], qa[ks][2], qa[ks][3], b2, b3);
     }
   }
 
@@ -131,7 +158,7 @@ __global__ void __launch_bounds__(kThreads) attn_mma_kernel(const AttnArgs a) {
   const float sl2 = a.scale * 1.4426950408889634f;
   float m0 = -INFINITY, m1 = -INFINITY;
 #pragma unroll
-  for (int j = 0; j < 16; ++j) {
+  for (int j = 0; j < kNT; ++j) {
     const bool v0 = sValid[8 * j + 2 * t] != 0, v1 = sValid[8 * j + 2 * t + 1] != 0;
     s[j][0] = v0 ? s[j][0] * sl2 : -INFINITY;
     s[j][1] = v1 ? s[j][1] * sl2 : -INFINITY;
@@ -148,7 +175,7 @@ __global__ void __launch_bounds__(kThreads) attn_mma_kernel(const AttnArgs a) {
   const float b1s = m1 == -INFINITY ? 0.f : m1;
   float l0 = 0.f, l1 = 0.f;
 #pragma unroll
-  for (int j = 0; j < 16; ++j) {
+  for (int j = 0; j < kNT; ++j) {
     s[j][0] = exp2f(s[j][0] - b0s);
     s[j][1] = exp2f(s[j][1] - b0s);
     s[j][2] = exp2f(s[j][2] - b1s);
@@ -162,9 +189,9 @@ __global__ void __launch_bounds__(kThreads) attn_mma_kernel(const AttnArgs a) {
   l1 += __shfl_xor_sync(0xffffffffu, l1, 2);
 
   // --- O = P V (P from the S accumulators, V rows via ldmatrix.trans)
-  float o[16][4];
+  float o[kDv / 8][4];
 #pragma unroll
-  for (int j = 0; j < 16; ++j) o[j][0] = o[j][1] = o[j][2] = o[j][3] = 0.f;
+  for (int j = 0; j < kDv / 8; ++j) o[j][0] = o[j][1] = o[j][2] = o[j][3] = 0.f;
   const uint8_t* vrow = sV + ((lane & 7) + 8 * ((lane >> 3) & 1)) * kVRow + (lane >> 4) * 16;
 #pragma unroll
   for (int kk = 0; kk < kSlots / 16; ++kk) {
@@ -185,7 +212,7 @@ __global__ void __launch_bounds__(kThreads) attn_mma_kernel(const AttnArgs a) {
   __syncthreads();
   const int h0 = warp * 16 + g, h1 = h0 + 8;
 #pragma unroll
-  for (int j = 0; j < 16; ++j) {
+  for (int j = 0; j < kDv / 8; ++j) {
     *reinterpret_cast<float2*>(sO + h0 * kORow + 8 * j + 2 * t) = make_float2(o[j][0], o[j][1]);
     *reinterpret_cast<float2*>(sO + h1 * kORow + 8 * j + 2 * t) = make_float2(o[j][2], o[j][3]);
   }
@@ -197,29 +224,41 @@ __global__ void __launch_bounds__(kThreads) attn_mma_kernel(const AttnArgs a) {
   }
   cluster_sync_all();
 
-  // --- merge the cluster's partials in CTA order; thread owns (head, dim) pairs
-  const int nthreads = int(ncta) * kThreads;
-  for (int e = int(crank) * kThreads + tid; e < kH * kDv; e += nthreads) {
-    const int h = e / kDv, d = e % kDv;
-    float mr[kMaxCluster];
+  // --- merge factors f_c[h] = exp2(m_c - M) / L for every CTA c (fixed order)
+  if (tid < kH) {
+    const int h = tid;
+    float mr[kMaxCluster], lr[kMaxCluster];
     float M = -INFINITY;
     for (uint32_t r = 0; r < ncta; ++r) {
       mr[r] = dsmem_ld_f32(dsmem_addr(sM + h, r));
+      lr[r] = dsmem_ld_f32(dsmem_addr(sL + h, r));
       M = fmaxf(M, mr[r]);
     }
-    float L = 0.f, O = 0.f;
-    if (M != -INFINITY) {
-      for (uint32_t r = 0; r < ncta; ++r) {
-        if (mr[r] == -INFINITY) continue;
-        const float f = exp2f(mr[r] - M);
-        L += f * dsmem_ld_f32(dsmem_addr(sL + h, r));
-        O += f * dsmem_ld_f32(dsmem_addr(sO + h * kORow + d, r));
-      }
-    }
-    const long long oi = ((long long)b * kH + h) * kDv + d;
-    a.out[oi] = M == -INFINITY ? 0.f : O / L;
-    if (d == 0 && a.lse != nullptr)
+    float L = 0.f;
+    for (uint32_t r = 0; r < ncta; ++r)
+      if (mr[r] != -INFINITY) L += exp2f(mr[r] - M) * lr[r];
+    for (uint32_t r = 0; r < ncta; ++r)
+      sF[r * kH + h] = (M == -INFINITY || mr[r] == -INFINITY) ? 0.f : exp2f(mr[r] - M) / L;
+    if (crank == 0 && a.lse != nullptr)
       a.lse[(long long)b * kH + h] = M == -INFINITY ? -INFINITY : (M + log2f(L)) * 0.6931471805599453f;
+  }
+  __syncthreads();
+
+  // --- out[h, 4d..4d+4) = sum_c f_c[h] * O_c[h, 4d..4d+4); thread owns float4 slices
+  const int nthreads = int(ncta) * kThreads;
+  for (int e = int(crank) * kThreads + tid; e < kH * kDv / 4; e += nthreads) {
+    const int h = e / (kDv / 4), d4 = e % (kDv / 4);
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (uint32_t r = 0; r < ncta; ++r) {
+      const float f = sF[r * kH + h];
+      float4 v;
+      dsmem_ld_v4(v, dsmem_addr(sO + h * kORow + 4 * d4, r));
+      acc.x += f * v.x;
+      acc.y += f * v.y;
+      acc.z += f * v.z;
+      acc.w += f * v.w;
+    }
+    *reinterpret_cast<float4*>(a.out + ((long long)b * kH + h) * kDv + 4 * d4) = acc;
   }
   cluster_sync_all();
 }

@@ -103,20 +103,44 @@ __global__ void __launch_bounds__(kThreads) topk_kernel(const TopkArgs a) {
   const int len = max(0, min(a.chunk, n - base));     // positions in this chunk
   const int p0 = tid * IPT;                           // first local position of this thread
 
+  // Independent, vectorised loads of this thread's IPT scores (and candidate ids).
   uint32_t key[IPT];
   uint32_t valid = 0;
+  const float* sp = a.scores + row + base + p0;
+  const int* cp = a.cand != nullptr ? a.cand + row + base + p0 : nullptr;
+  const int nloc = max(0, min(IPT, len - p0));
+  float sv[IPT];
+  int cv[IPT];
+  const bool vec = nloc == IPT &&
+                   ((reinterpret_cast<uintptr_t>(sp) | reinterpret_cast<uintptr_t>(cp)) & 15u) == 0;
+  if (vec) {
+#pragma unroll
+    for (int i = 0; i < IPT; i += 4) {
+      const float4 v = *reinterpret_cast<const float4*>(sp + i);
+      sv[i] = v.x; sv[i + 1] = v.y; sv[i + 2] = v.z; sv[i + 3] = v.w;
+    }
+    if (cp != nullptr) {
+#pragma unroll
+      for (int i = 0; i < IPT; i += 4) {
+        const int4 v = *reinterpret_cast<const int4*>(cp + i);
+        cv[i] = v.x; cv[i + 1] = v.y; cv[i + 2] = v.z; cv[i + 3] = v.w;
+      }
+    } else {
+#pragma unroll
+      for (int i = 0; i < IPT; ++i) cv[i] = 0;
+    }
+  } else {
+#pragma unroll
+    for (int i = 0; i < IPT; ++i) {
+      sv[i] = i < nloc ? sp[i] : 0.f;
+      cv[i] = (cp != nullptr && i < nloc) ? cp[i] : 0;
+    }
+  }
 #pragma unroll
   for (int i = 0; i < IPT; ++i) {
-    key[i] = 0u;
-    const int lp = p0 + i;
-    if (lp < len) {
-      const long long pos = row + base + lp;
-      const bool ok = a.cand == nullptr || a.cand[pos] >= 0;
-      if (ok) {
-        key[i] = score_key(a.scores[pos]);
-        valid |= 1u << i;
-      }
-    }
+    const bool ok = i < nloc && cv[i] >= 0;
+    key[i] = ok ? score_key(sv[i]) : 0u;
+    valid |= ok ? (1u << i) : 0u;
   }
   const uint32_t n_valid = block_sum(__popc(valid), sm.warp_a);
   const uint32_t k = uint32_t(a.k);
