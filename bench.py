@@ -287,6 +287,20 @@ def run_reference(args):
     return 0
 
 
+def make_flusher(torch, nbytes, device):
+    """L2 flush between timed steps: write a buffer larger than L2, then read it
+    back, so the next step finds none of its inputs in L2 and no dirty lines
+    whose write-back would be charged to it."""
+    buf = torch.empty(nbytes, dtype=torch.uint8, device=device)
+    view = buf.view(torch.int64)
+    sink = torch.empty((), dtype=torch.int64, device=device)
+
+    def flush():
+        buf.fill_(1)
+        torch.amax(view, dim=0, out=sink)
+    return flush
+
+
 def config_of(wl, args):
     sh = wl.shape
     spec = W.WORKLOADS.get(wl.name, {})
@@ -294,7 +308,8 @@ def config_of(wl, args):
             "entries": sh.n_entries, "layers": [W.MODE_NAMES[L.mode] + ("+hier" if L.hier else "") for L in wl.layers],
             "pool_blocks": sh.pool_blocks, "topk": sh.topk, "swa": sh.swa, "q_heads": sh.q_heads,
             "k_dim": sh.k_dim, "v_dim": sh.v_dim, "idx_heads": sh.idx_heads, "idx_dim": sh.idx_dim,
-            "l2": f"flushed between timed steps ({args.flush_mb} MB write)", "launch": "CUDA graph replay"}
+            "l2": f"flushed between timed steps ({args.flush_mb} MB written then read back)",
+            "launch": "CUDA graph replay"}
 
 
 # ----------------------------------------------------------------------------- GPU arm
@@ -328,7 +343,7 @@ def run_ours(args):
     call = csa2.LayerGroupCall(sh, d["layers"], d["k_main"], d["v_main"], d["k_idx"], d["kb"], d["n_valid"],
                                d["n_swa"], d["ws"])
     stream = torch.cuda.Stream(device=dev)
-    flush = torch.empty(args.flush_mb * 1024 * 1024, dtype=torch.uint8, device=dev)
+    flush = make_flusher(torch, args.flush_mb * 1024 * 1024, dev)
     with torch.cuda.stream(stream):
         call(stream)                                     # first call: attributes, validation
         torch.cuda.synchronize()
@@ -338,7 +353,7 @@ def run_ours(args):
             call(stream)
         per_step_launches = csa2.launch_count() - n0
         for _ in range(args.warmup):
-            flush.zero_()
+            flush()
             graph.replay()
         torch.cuda.synchronize()
         st, bits = csa2.read_device_error(d["ws"], stream)
@@ -347,16 +362,29 @@ def run_ours(args):
 
         evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
                for _ in range(args.steps)]
-        barrier()
-        torch.cuda.synchronize()
+
+        def soak(seconds):
+            # untimed replays of the same step so that nvidia-smi (200 ms period) sees the
+            # clocks of this workload around the (short) timed region
+            t_end = time.perf_counter() + seconds
+            while time.perf_counter() < t_end:
+                for _ in range(20):
+                    flush()
+                    graph.replay()
+                torch.cuda.synchronize()
+
         with ClockSampler(dev.index) as clk:
+            soak(args.clock_soak)
+            barrier()
+            torch.cuda.synchronize()
             for e0, e1 in evs:
-                flush.zero_()
+                flush()
                 e0.record(stream)
                 graph.replay()
                 e1.record(stream)
             torch.cuda.synchronize()
-        barrier()
+            barrier()
+            soak(args.clock_soak / 2)
         step_ms = [e0.elapsed_time(e1) for e0, e1 in evs]
     total_s = max_over_ranks(sum(step_ms) / 1e3, dev)
     value = sh.batch * world * args.steps / total_s
@@ -367,6 +395,8 @@ def run_ours(args):
     step_gbs = ab["total"] / (ms_per_step / 1e3) / 1e9
     e2e = end_to_end(csa2, wl, d, graph, stream, flush, args, dev)
     clocks = clk.summary()
+    clocks["window"] = (f"nvidia-smi every 200 ms over the timed steps plus {args.clock_soak:.1f} s before and "
+                        f"{args.clock_soak / 2:.1f} s after of untimed replays of the same step")
 
     cpu = None
     if pool is not None:
@@ -430,7 +460,7 @@ def dominant_kernel_roofline(csa2, wl, d, stream, flush, args, peak, peak_src):
         torch.cuda.synchronize()
         ms = []
         for _ in range(reps):
-            flush.zero_()
+            flush()
             e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
             e0.record(stream)
             launch()
@@ -468,7 +498,7 @@ def end_to_end(csa2, wl, d, graph, stream, flush, args, dev):
     ms = []
     with torch.cuda.stream(stream):
         for i in range(args.warmup + steps):
-            flush.zero_()
+            flush()
             e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
             e0.record(stream)
             for hd, dd in zip(host_in, ins):
@@ -496,6 +526,8 @@ def main(argv=None):
     ap.add_argument("--workload", default="reindex_b64_128k", choices=sorted(W.WORKLOADS))
     ap.add_argument("--flush-mb", type=int, default=512)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--clock-soak", type=float, default=1.5,
+                    help="seconds of untimed replays around the timed steps while clocks are sampled")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")

@@ -171,12 +171,15 @@ int do_index_pooled(const csa2_shape& s, const void* q_idx, const float* w, cons
   return cuda_status(launch_indexer(a, true, pooled_fast(s), s.batch, s.pool_blocks, st));
 }
 
-// Multi-level exact Top-k: chunks of <= topk_max_chunk() positions, then merges.
+// Exact Top-k: rows longer than one cluster can hold are first cut into chunks
+// of <= topk_max_chunk() positions whose Top-k lists are merged, then one
+// cluster launch selects the final Top-k.
 int do_topk(const csa2_shape& s, const WsLayout& L, void* ws, const float* scores, int64_t ld,
             const int32_t* cand, const int32_t* n_cand, int64_t n_cap, int k, int32_t* idx_out,
             float* score_out, int32_t* n_out, cudaStream_t st) {
   int* err = at<int>(ws, L.hdr);
   const int64_t maxc = topk_max_chunk();
+  const int64_t maxcl = topk_cluster_max();
   TopkArgs a{};
   a.scores = scores;
   a.ld_in = ld;
@@ -188,7 +191,7 @@ int do_topk(const csa2_shape& s, const WsLayout& L, void* ws, const float* score
   a.err = err;
   int64_t n = n_cap;
   bool use_a = true;
-  while (n > maxc) {
+  while (n > maxcl) {
     const int64_t chunks = ceil_div(n, maxc);
     a.chunk = int(ceil_div(n, chunks));
     a.idx_out = at<int32_t>(ws, use_a ? L.tk_ids_a : L.tk_ids_b);
@@ -205,11 +208,12 @@ int do_topk(const csa2_shape& s, const WsLayout& L, void* ws, const float* score
     a.n_cap = int(n);
     use_a = !use_a;
   }
-  a.chunk = int(n > 0 ? n : 1);
+  a.n_cap = int(n > 0 ? n : 1);
+  if (a.n_cand == nullptr) a.n_fixed = int(n);
   a.idx_out = idx_out;
   a.score_out = score_out;
   a.n_out = n_out;
-  return cuda_status(launch_topk(a, 1, s.batch, st));
+  return cuda_status(launch_topk_cluster(a, s.batch, st));
 }
 
 int do_attn(const csa2_shape& s, const void* q, const void* k_main, const void* v_main, const int32_t* idx,
@@ -237,10 +241,36 @@ int do_attn(const csa2_shape& s, const void* q, const void* k_main, const void* 
   return cuda_status(launch_attn(a, attn_fast(s), s.batch, st));
 }
 
+SelectArgs select_args(const csa2_shape& s, const void* keys, int64_t rows_per_seq, const void* q_idx,
+                       const float* w, const int32_t* n_valid, int div, int k, int32_t* out, int64_t ld_out,
+                       int32_t* n_out, int* err) {
+  SelectArgs a{};
+  a.keys = keys;
+  a.rows_per_seq = rows_per_seq;
+  a.q_idx = q_idx;
+  a.w = w;
+  a.relu = s.relu;
+  a.n_valid = n_valid;
+  a.valid_cap = s.n_entries;
+  a.div = div;
+  a.k = k;
+  a.out = out;
+  a.ld_out = ld_out;
+  a.n_out = n_out;
+  a.err = err;
+  return a;
+}
+
 int do_index_blocks(const csa2_shape& s, const WsLayout& L, void* ws, const void* q_idx, const float* w,
                     const void* kb, const int32_t* n_valid, int32_t* pool_out, int32_t* n_pool_out,
                     cudaStream_t st) {
   int* err = at<int>(ws, L.hdr);
+  if (indexer_fast(s) && index_select_supported(false, int(L.nb_cap))) {
+    // fused: block scoring and pool selection in one cluster launch
+    SelectArgs a = select_args(s, kb, L.nb_cap, q_idx, w, n_valid, s.block, s.pool_blocks, pool_out,
+                               s.pool_blocks, n_pool_out, err);
+    return cuda_status(launch_index_select(a, false, s.batch, int(L.nb_cap), st));
+  }
   float* bs = at<float>(ws, L.blk_scores);
   int32_t* nblk = at<int32_t>(ws, L.n_blk);
   CSA2_TRY(do_index_flat(s, q_idx, w, kb, L.nb_cap, n_valid, s.block, bs, nullptr, nblk, L.nb_cap, err, st));
@@ -409,9 +439,24 @@ int csa2_layer_group(const csa2_shape* shape, const csa2_layer* layers, int32_t 
         int32_t* pool = at<int32_t>(ws, L.pool);
         int32_t* npool = at<int32_t>(ws, L.n_pool);
         CSA2_TRY(do_index_blocks(s, L, ws, y.q_idx, y.w_idx, kb, n_valid, pool, npool, stream));
-        CSA2_TRY(do_index_pooled(s, y.q_idx, y.w_idx, k_idx, n_valid, pool, npool, ts, tc, nc, err, stream));
-        const int64_t ld = int64_t(s.pool_blocks) * s.block;
-        CSA2_TRY(do_topk(s, L, ws, ts, ld, tc, nc, ld, s.topk, dst, nullptr, nullptr, stream));
+        if (pooled_fast(s) && index_select_supported(true, s.pool_blocks)) {
+          // fused: pooled token scoring and Top-K in one cluster launch
+          SelectArgs a = select_args(s, k_idx, s.n_entries, y.q_idx, y.w_idx, n_valid, 1, s.topk, dst, s.topk,
+                                     nullptr, err);
+          a.pool = pool;
+          a.n_pool = npool;
+          a.pool_cap = s.pool_blocks;
+          CSA2_TRY(cuda_status(launch_index_select(a, true, s.batch, s.pool_blocks, stream)));
+        } else {
+          CSA2_TRY(do_index_pooled(s, y.q_idx, y.w_idx, k_idx, n_valid, pool, npool, ts, tc, nc, err, stream));
+          const int64_t ld = int64_t(s.pool_blocks) * s.block;
+          CSA2_TRY(do_topk(s, L, ws, ts, ld, tc, nc, ld, s.topk, dst, nullptr, nullptr, stream));
+        }
+      } else if (indexer_fast(s) && index_select_supported(false, s.n_entries)) {
+        // fused: flat token scoring and Top-K in one cluster launch
+        SelectArgs a = select_args(s, k_idx, s.n_entries, y.q_idx, y.w_idx, n_valid, 1, s.topk, dst, s.topk,
+                                   nullptr, err);
+        CSA2_TRY(cuda_status(launch_index_select(a, false, s.batch, s.n_entries, stream)));
       } else {
         CSA2_TRY(do_index_flat(s, y.q_idx, y.w_idx, k_idx, s.n_entries, n_valid, 1, ts, nullptr, nc, s.n_entries,
                                err, stream));

@@ -42,9 +42,11 @@ constexpr int kOffL = kOffM + kH * 4;
 constexpr int kOffF = kOffL + kH * 4;             // [kMaxCluster][kH] merge factors
 constexpr int kOffValid = kOffF + kMaxCluster * kH * 4;
 constexpr int kOffBar = kOffValid + kSlots * 4;
-constexpr int kSmemBytes = kOffBar + 16;
+constexpr int kSmemBytes = kOffBar + 2 * 8;
+constexpr int kHalf = kSlots / 2;                 // slots per gather barrier (80)
 static_assert(kH * kORow * 4 <= kSlots * kKRow, "partial O must fit in the K region");
 static_assert(kSlots % 16 == 0, "PV k-steps need 16-key groups");
+static_assert(kNT % 4 == 0, "each gather half covers whole n-tile pairs");
 
 CSA2_DEV void dsmem_ld_v4(float4& v, uint32_t addr) {
   asm volatile("ld.shared::cluster.v4.f32 {%0,%1,%2,%3}, [%4];"
@@ -69,14 +71,33 @@ __global__ void __launch_bounds__(kThreads, 2) attn_mma_kernel(const AttnArgs a)
   const int g = lane >> 2, t = lane & 3;
   const uint32_t crank = cluster_rank(), ncta = cluster_size();
 
+  pdl_launch_dependents();
   if (tid == 0) {
-    mbar_init(bar, kThreads);
+    mbar_init(&bar[0], kThreads);
+    mbar_init(&bar[1], kThreads);
     mbar_fence_init();
   }
+  // --- Q A-fragments for heads 16w + g and 16w + g + 8, straight from global
+  uint32_t qa[kDk / 16][4];
+  {
+    const uint32_t* q0 = reinterpret_cast<const uint32_t*>(static_cast<const uint8_t*>(a.q) +
+                                                           ((long long)b * kH + warp * 16 + g) * (kDk * 2)) + t;
+    const uint32_t* q1 = q0 + 8 * (kDk / 2);
+#pragma unroll
+    for (int ks = 0; ks < kDk / 16; ++ks) {
+      qa[ks][0] = __ldg(q0 + ks * 8);
+      qa[ks][1] = __ldg(q1 + ks * 8);
+      qa[ks][2] = __ldg(q0 + ks * 8 + 4);
+      qa[ks][3] = __ldg(q1 + ks * 8 + 4);
+    }
+  }
+  pdl_wait();   // the indices come from the preceding launch
   __syncthreads();
 
-  // --- gather: thread `tid` owns key slots tid and tid + 128 of this CTA
-  uint32_t tx = 0;
+  // --- gather: thread `tid` owns key slots tid and tid + 128 of this CTA; slots
+  // [0, 80) complete on bar[0] and [80, 160) on bar[1], so the first half can be
+  // scored while the second is still arriving
+  uint32_t tx0 = 0u, tx1 = 0u;
   const uint8_t* ksrc[2] = {nullptr, nullptr};
   const uint8_t* vsrc[2] = {nullptr, nullptr};
   const int ns = clamp_count(a.n_swa[b], a.swa, a.err);
@@ -99,58 +120,52 @@ __global__ void __launch_bounds__(kThreads, 2) attn_mma_kernel(const AttnArgs a)
       vsrc[j] = static_cast<const uint8_t*>(a.v_swa) + r * (kDv * 2);
     }
     sValid[ls] = ksrc[j] != nullptr ? 1 : 0;
-    if (ksrc[j] != nullptr) tx += kDk * 2 + kDv * 2;
+    if (ksrc[j] != nullptr) {
+      if (ls < kHalf)
+        tx0 += kDk * 2 + kDv * 2;
+      else
+        tx1 += kDk * 2 + kDv * 2;
+    }
   }
-  mbar_arrive_expect_tx(bar, tx);
+  mbar_arrive_expect_tx(&bar[0], tx0);
+  mbar_arrive_expect_tx(&bar[1], tx1);
 #pragma unroll
   for (int j = 0; j < 2; ++j) {
     const int ls = tid + j * kThreads;
     if (ls >= kSlots) break;
+    uint64_t* hb = &bar[ls < kHalf ? 0 : 1];
     if (ksrc[j] != nullptr) {
-      bulk_g2s(sK + ls * kKRow, ksrc[j], kDk * 2, bar);
-      bulk_g2s(sV + ls * kVRow, vsrc[j], kDv * 2, bar);
+      bulk_g2s(sK + ls * kKRow, ksrc[j], kDk * 2, hb);
+      bulk_g2s(sV + ls * kVRow, vsrc[j], kDv * 2, hb);
     } else {
       const uint4 z = make_uint4(0u, 0u, 0u, 0u);
       for (int i = 0; i < kDk * 2; i += 16) *reinterpret_cast<uint4*>(sK + ls * kKRow + i) = z;
       for (int i = 0; i < kDv * 2; i += 16) *reinterpret_cast<uint4*>(sV + ls * kVRow + i) = z;
     }
   }
+  __syncthreads();   // zero-filled rows and slot flags visible to every warp
 
-  // --- Q A-fragments for heads 16w + g and 16w + g + 8, straight from global
-  uint32_t qa[kDk / 16][4];
-  {
-    const uint32_t* q0 = reinterpret_cast<const uint32_t*>(static_cast<const uint8_t*>(a.q) +
-                                                           ((long long)b * kH + warp * 16 + g) * (kDk * 2)) + t;
-    const uint32_t* q1 = q0 + 8 * (kDk / 2);
-#pragma unroll
-    for (int ks = 0; ks < kDk / 16; ++ks) {
-      qa[ks][0] = __ldg(q0 + ks * 8);
-      qa[ks][1] = __ldg(q1 + ks * 8);
-      qa[ks][2] = __ldg(q0 + ks * 8 + 4);
-      qa[ks][3] = __ldg(q1 + ks * 8 + 4);
-    }
-  }
-  const bool ok = mbar_wait(bar, 0);
-  if (!ok) {
-    // record the stall, give the copies in flight one more bounded wait
-    report(a.err, kErrTimeout, b);
-    mbar_wait(bar, 0);
-  }
-  __syncthreads();
-
-  // --- S = Q K^T for heads [16w, 16w + 16) x 160 keys
+  // --- S = Q K^T for heads [16w, 16w + 16) x 160 keys, one half per gather barrier
   float s[kNT][4];
 #pragma unroll
   for (int j = 0; j < kNT; ++j) s[j][0] = s[j][1] = s[j][2] = s[j][3] = 0.f;
   const uint8_t* krow = sK + ((lane & 7) + 8 * (lane >> 4)) * kKRow + ((lane >> 3) & 1) * 16;
 #pragma unroll
-  for (int ks = 0; ks < kDk / 16; ++ks) {
+  for (int half = 0; half < 2; ++half) {
+    if (!mbar_wait(&bar[half], 0)) {
+      // record the stall, give the copies in flight one more bounded wait
+      report(a.err, kErrTimeout, b);
+      mbar_wait(&bar[half], 0);
+    }
 #pragma unroll
-    for (int jp = 0; jp < kNT / 2; ++jp) {
-      uint32_t b0, b1, b2, b3;
-      ldsm_x4(b0, b1, b2, b3, krow + jp * 16 * kKRow + ks * 32);
-      mma_bf16(s[2 * jp], qa[ks][0], qa[ks][1], qa[ks][2], qa[ks][3], b0, b1);
-      mma_bf16(s[2 * jp + 1], qa[ks][0], qa[ks][1], qa[ks][2], qa[ks][3], b2, b3);
+    for (int ks = 0; ks < kDk / 16; ++ks) {
+#pragma unroll
+      for (int jp = half * kNT / 4; jp < (half + 1) * kNT / 4; ++jp) {
+        uint32_t b0, b1, b2, b3;
+        ldsm_x4(b0, b1, b2, b3, krow + jp * 16 * kKRow + ks * 32);
+        mma_bf16(s[2 * jp], qa[ks][0], qa[ks][1], qa[ks][2], qa[ks][3], b0, b1);
+        mma_bf16(s[2 * jp + 1], qa[ks][0], qa[ks][1], qa[ks][2], qa[ks][3], b2, b3);
+      }
     }
   }
 
@@ -224,41 +239,68 @@ __global__ void __launch_bounds__(kThreads, 2) attn_mma_kernel(const AttnArgs a)
   }
   cluster_sync_all();
 
-  // --- merge factors f_c[h] = exp2(m_c - M) / L for every CTA c (fixed order)
+  // --- merge factors f_c[h] = exp2(m_c - M) / L for every CTA c (fixed order);
+  // all remote loads are issued before any of them is used
   if (tid < kH) {
     const int h = tid;
     float mr[kMaxCluster], lr[kMaxCluster];
-    float M = -INFINITY;
-    for (uint32_t r = 0; r < ncta; ++r) {
-      mr[r] = dsmem_ld_f32(dsmem_addr(sM + h, r));
-      lr[r] = dsmem_ld_f32(dsmem_addr(sL + h, r));
-      M = fmaxf(M, mr[r]);
+#pragma unroll
+    for (int r = 0; r < kMaxCluster; ++r) {
+      if (r < int(ncta)) {
+        mr[r] = dsmem_ld_f32(dsmem_addr(sM + h, r));
+        lr[r] = dsmem_ld_f32(dsmem_addr(sL + h, r));
+      } else {
+        mr[r] = -INFINITY;
+        lr[r] = 0.f;
+      }
     }
+    float M = -INFINITY;
+#pragma unroll
+    for (int r = 0; r < kMaxCluster; ++r) M = fmaxf(M, mr[r]);
     float L = 0.f;
-    for (uint32_t r = 0; r < ncta; ++r)
+#pragma unroll
+    for (int r = 0; r < kMaxCluster; ++r)
       if (mr[r] != -INFINITY) L += exp2f(mr[r] - M) * lr[r];
-    for (uint32_t r = 0; r < ncta; ++r)
-      sF[r * kH + h] = (M == -INFINITY || mr[r] == -INFINITY) ? 0.f : exp2f(mr[r] - M) / L;
+#pragma unroll
+    for (int r = 0; r < kMaxCluster; ++r)
+      if (r < int(ncta)) sF[r * kH + h] = (M == -INFINITY || mr[r] == -INFINITY) ? 0.f : exp2f(mr[r] - M) / L;
     if (crank == 0 && a.lse != nullptr)
       a.lse[(long long)b * kH + h] = M == -INFINITY ? -INFINITY : (M + log2f(L)) * 0.6931471805599453f;
   }
   __syncthreads();
 
-  // --- out[h, 4d..4d+4) = sum_c f_c[h] * O_c[h, 4d..4d+4); thread owns float4 slices
+  // --- out[h, 4d..4d+4) = sum_c f_c[h] * O_c[h, 4d..4d+4); thread owns float4 slices.
+  // The cluster has ncta * 128 threads and 64 * 32 slices: with ncta = 4 every
+  // thread owns exactly 4 slices; all their remote loads are issued up front.
+  constexpr int kSlices = kH * kDv / 4;
   const int nthreads = int(ncta) * kThreads;
-  for (int e = int(crank) * kThreads + tid; e < kH * kDv / 4; e += nthreads) {
-    const int h = e / (kDv / 4), d4 = e % (kDv / 4);
-    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-    for (uint32_t r = 0; r < ncta; ++r) {
-      const float f = sF[r * kH + h];
-      float4 v;
-      dsmem_ld_v4(v, dsmem_addr(sO + h * kORow + 4 * d4, r));
-      acc.x += f * v.x;
-      acc.y += f * v.y;
-      acc.z += f * v.z;
-      acc.w += f * v.w;
+  for (int e0 = int(crank) * kThreads + tid; e0 < kSlices; e0 += 4 * nthreads) {
+    float4 v[4][kMaxCluster];
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      const int e = e0 + u * nthreads;
+      const int h = e / (kDv / 4), d4 = e % (kDv / 4);
+#pragma unroll
+      for (int r = 0; r < kMaxCluster; ++r)
+        if (e < kSlices && r < int(ncta)) dsmem_ld_v4(v[u][r], dsmem_addr(sO + h * kORow + 4 * d4, r));
     }
-    *reinterpret_cast<float4*>(a.out + ((long long)b * kH + h) * kDv + 4 * d4) = acc;
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      const int e = e0 + u * nthreads;
+      if (e >= kSlices) break;
+      const int h = e / (kDv / 4), d4 = e % (kDv / 4);
+      float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+      for (int r = 0; r < kMaxCluster; ++r) {
+        if (r >= int(ncta)) break;
+        const float f = sF[r * kH + h];
+        acc.x += f * v[u][r].x;
+        acc.y += f * v[u][r].y;
+        acc.z += f * v[u][r].z;
+        acc.w += f * v[u][r].w;
+      }
+      *reinterpret_cast<float4*>(a.out + ((long long)b * kH + h) * kDv + 4 * d4) = acc;
+    }
   }
   cluster_sync_all();
 }
@@ -267,6 +309,8 @@ __global__ void __launch_bounds__(kThreads, 2) attn_mma_kernel(const AttnArgs a)
 __global__ void __launch_bounds__(128) attn_generic_kernel(const AttnArgs a) {
   extern __shared__ float sh[];
   const int b = blockIdx.y, h = blockIdx.x, tid = threadIdx.x;
+  pdl_launch_dependents();
+  pdl_wait();
   const int nslots = a.topk + a.swa;
   float* sq = sh;                       // [k_dim]
   float* sp = sh + a.k_dim;             // [nslots] logits -> probabilities
@@ -346,8 +390,7 @@ cudaError_t launch_attn(const AttnArgs& a, bool fast, int batch, cudaStream_t st
     const size_t smem = (size_t(a.k_dim) + a.topk + a.swa + 32) * sizeof(float);
     dim3 grid(unsigned(a.heads), unsigned(batch));
     note_launch();
-    attn_generic_kernel<<<grid, 128, smem, st>>>(a);
-    return cudaGetLastError();
+    return launch_pdl(attn_generic_kernel, grid, dim3(128), smem, st, 1, a);
   }
   static bool attr_set = false;
   if (!attr_set) {
@@ -356,20 +399,9 @@ cudaError_t launch_attn(const AttnArgs& a, bool fast, int batch, cudaStream_t st
     attr_set = true;
   }
   const int ncta = (a.topk + a.swa + kSlots - 1) / kSlots;
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(unsigned(ncta), unsigned(batch), 1);
-  cfg.blockDim = dim3(kThreads, 1, 1);
-  cfg.dynamicSmemBytes = kSmemBytes;
-  cfg.stream = st;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeClusterDimension;
-  attr[0].val.clusterDim.x = unsigned(ncta);
-  attr[0].val.clusterDim.y = 1;
-  attr[0].val.clusterDim.z = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
   note_launch();
-  return cudaLaunchKernelEx(&cfg, attn_mma_kernel, a);
+  return launch_pdl(attn_mma_kernel, dim3(unsigned(ncta), unsigned(batch), 1), dim3(kThreads), kSmemBytes, st,
+                    unsigned(ncta), a);
 }
 
 int attn_max_cluster() { return kMaxCluster; }

@@ -99,6 +99,22 @@ CSA2_DEV void bulk_g2s(void* dst, const void* src, uint32_t bytes, uint64_t* bar
       : "memory");
 }
 
+CSA2_DEV void mbar_arrive(uint64_t* bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
+
+// ------------------------------------------------------------------ programmatic dependent launch
+
+// Wait until the preceding kernel in the stream has completed and its memory
+// is visible (no-op when the kernel was launched without the programmatic
+// serialization attribute).  Must precede any access to data that kernel
+// produces or consumes.
+CSA2_DEV void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
+// Allow the next kernel in the stream to be scheduled (it still waits in
+// pdl_wait for this kernel to complete).
+CSA2_DEV void pdl_launch_dependents() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
 // ------------------------------------------------------------------ MMA
 
 // D += A * B with A 16x16 (row), B 16x8 (col), bf16 inputs, fp32 accumulators.

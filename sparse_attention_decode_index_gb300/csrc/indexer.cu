@@ -8,13 +8,16 @@
 //
 // Fast path (bf16, 8 heads x 64 dims): the per-query product q_idx . K^T is a
 // dense [8 x 64] x [64 x n] contraction, computed with mma.sync m16n8k16 (16
-// entries x 8 heads x 16 dims per instruction).  Key rows (128 B each) are
-// streamed into a 4-stage shared-memory ring by bulk (TMA) copies completing
-// on mbarriers: one copy per 128-row tile in flat mode, one per 8-entry block
-// (1 KB) in pooled mode.  Each thread reads the 32 contiguous bytes of a row
-// that its fragment needs, so no ldmatrix or swizzle is required: the dim
-// order inside a k-step is permuted identically for the A (keys) and B
-// (q_idx) fragments, which leaves the dot products unchanged.
+// entries x 8 heads x 16 dims per instruction).  The kernel is warp
+// specialized: one producer warp streams key rows (128 B each) into a 4-stage
+// shared-memory ring with bulk (TMA) copies completing on "full" mbarriers --
+// one 16 KB copy per 128-row tile in flat mode, one 1 KB copy per 8-entry
+// block in pooled mode, issued by 16 lanes in parallel -- and four consumer
+// warps score the rows, releasing each stage on an "empty" mbarrier as soon as
+// their fragments are in registers.  Each consumer thread reads the 32
+// contiguous bytes of a row that its fragment needs: the dim order inside a
+// k-step is permuted identically for the A (keys) and B (q_idx) fragments,
+// which leaves the dot products unchanged, so no ldmatrix or swizzle is needed.
 #include "common.cuh"
 #include "internal.h"
 
@@ -28,13 +31,15 @@ constexpr int kRowBytes = kDim * 2;                  // 128
 constexpr int kTileRows = 128;
 constexpr int kTileBytes = kTileRows * kRowBytes;    // 16 KB
 constexpr int kStages = 4;
-constexpr int kThreads = 128;
+constexpr int kConsumers = 4;                        // consumer warps (2 m-tiles of 16 rows each per tile)
+constexpr int kThreads = (kConsumers + 1) * 32;      // + one producer warp
 constexpr int kBlock = 8;                            // entries per block (pooled fast path)
+constexpr int kBlockBytes = kBlock * kRowBytes;      // 1 KB
 constexpr int kBlocksPerTile = kTileRows / kBlock;   // 16
 constexpr int kMaxPoolSlice = 2048;                  // pool positions per CTA held in smem
 
 constexpr size_t kSmemTiles = size_t(kStages) * kTileBytes;
-constexpr size_t kSmemBars = 64;
+constexpr size_t kSmemBars = 2 * kStages * sizeof(uint64_t);
 constexpr size_t fast_smem_bytes(bool pooled) {
   return kSmemTiles + kSmemBars + (pooled ? kMaxPoolSlice * sizeof(int) : 0);
 }
@@ -44,13 +49,23 @@ __global__ void __launch_bounds__(kThreads) indexer_mma_kernel(const IndexerArgs
   extern __shared__ __align__(1024) uint8_t smem[];
   uint8_t* tiles = smem;
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + kSmemTiles);
+  uint64_t* empty = full + kStages;
   int* s_pool = reinterpret_cast<int*>(smem + kSmemTiles + kSmemBars);
 
   const int b = blockIdx.y;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const int g = lane >> 2, t = lane & 3;
+  pdl_launch_dependents();
 
   const int nv = clamp_count(a.n_valid[b], a.valid_cap, a.err);
+  if (tid == 0) {
+    for (int s = 0; s < kStages; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], kConsumers);
+    }
+    mbar_fence_init();
+  }
+  pdl_wait();   // the pool / n_pool come from the preceding launch
+
   int begin, end;
   if (!POOLED) {
     const int n = (nv + a.div - 1) / a.div;
@@ -76,44 +91,49 @@ __global__ void __launch_bounds__(kThreads) indexer_mma_kernel(const IndexerArgs
       s_pool[i] = blk;
     }
   }
-  if (tid == 0) {
-    for (int s = 0; s < kStages; ++s) mbar_init(&full[s], 1);
-    mbar_fence_init();
-  }
   __syncthreads();
 
   const int rows_total = POOLED ? (end - begin) * kBlock : (end - begin);
   const int ntiles = (rows_total + kTileRows - 1) / kTileRows;
-  const uint8_t* keys =
-      static_cast<const uint8_t*>(a.keys) + (long long)b * a.rows_per_seq * kRowBytes;
+  const uint8_t* keys = static_cast<const uint8_t*>(a.keys) + (long long)b * a.rows_per_seq * kRowBytes;
 
-  auto issue = [&](int tile) {
-    const int s = tile % kStages;
-    uint8_t* dst = tiles + s * kTileBytes;
-    if (!POOLED) {
-      const int r0 = begin + tile * kTileRows;
-      const int rows = min(kTileRows, end - r0);
-      const uint32_t bytes = uint32_t(rows) * kRowBytes;
-      mbar_arrive_expect_tx(&full[s], bytes);
-      bulk_g2s(dst, keys + (long long)r0 * kRowBytes, bytes, &full[s]);
-    } else {
-      const int p0 = tile * kBlocksPerTile;
-      const int np = min(kBlocksPerTile, (end - begin) - p0);
-      uint32_t bytes = 0;
-      for (int i = 0; i < np; ++i) bytes += (s_pool[p0 + i] >= 0) ? kBlock * kRowBytes : 0;
-      mbar_arrive_expect_tx(&full[s], bytes);
-      for (int i = 0; i < np; ++i) {
-        const int blk = s_pool[p0 + i];
+  if (warp == kConsumers) {
+    // ---------------- producer warp
+    int i = 0;
+    for (; i < ntiles; ++i) {
+      const int s = i % kStages;
+      bool ok = true;
+      if (lane == 0 && i >= kStages) ok = mbar_wait(&empty[s], ((i / kStages) - 1) & 1);
+      if (!__shfl_sync(0xffffffffu, ok, 0)) break;
+      uint8_t* dst = tiles + s * kTileBytes;
+      if (!POOLED) {
+        if (lane == 0) {
+          const int r0 = begin + i * kTileRows;
+          const uint32_t bytes = uint32_t(min(kTileRows, end - r0)) * kRowBytes;
+          mbar_arrive_expect_tx(&full[s], bytes);
+          bulk_g2s(dst, keys + (long long)r0 * kRowBytes, bytes, &full[s]);
+        }
+      } else {
+        const int p0 = i * kBlocksPerTile;
+        const int np = min(kBlocksPerTile, (end - begin) - p0);
+        const int blk = lane < np ? s_pool[p0 + lane] : -1;
+        const unsigned have = __ballot_sync(0xffffffffu, blk >= 0);
+        if (lane == 0) mbar_arrive_expect_tx(&full[s], uint32_t(__popc(have)) * kBlockBytes);
+        __syncwarp();
         if (blk >= 0)
-          bulk_g2s(dst + i * kBlock * kRowBytes, keys + (long long)blk * kBlock * kRowBytes,
-                   kBlock * kRowBytes, &full[s]);
+          bulk_g2s(dst + lane * kBlockBytes, keys + (long long)blk * kBlockBytes, kBlockBytes, &full[s]);
       }
     }
-  };
-  if (tid == 0) {
-    for (int i = 0; i < min(kStages, ntiles); ++i) issue(i);
+    if (lane == 0) {
+      if (i < ntiles) report(a.err, kErrTimeout, i);
+      // let every copy this CTA issued land (bounded) before its shared memory is released
+      for (int j = max(0, i - kStages); j < i; ++j) mbar_wait(&full[j % kStages], (j / kStages) & 1);
+    }
+    return;
   }
 
+  // ---------------- consumer warps
+  const int g = lane >> 2, t = lane & 3;
   // B fragments (q_idx^T, 16 dims x 8 heads per k-step): thread (g, t) holds
   // q[head g][16t .. 16t + 16).  For k-step s its k-slots {2t, 2t+1} are dims
   // 16t + 4s + {0, 1} and {2t+8, 2t+9} are dims 16t + 4s + {2, 3}; the A
@@ -128,68 +148,67 @@ __global__ void __launch_bounds__(kThreads) indexer_mma_kernel(const IndexerArgs
   float* scores = a.scores + (long long)b * a.ld;
   int* cand = a.cand != nullptr ? a.cand + (long long)b * a.ld : nullptr;
 
-  int i = 0;
-  for (; i < ntiles; ++i) {
+  for (int i = 0; i < ntiles; ++i) {
     const int s = i % kStages;
-    const bool ok = mbar_wait(&full[s], (i / kStages) & 1);
-    if (ok) {
-      const uint8_t* tile = tiles + s * kTileBytes;
-      const int tile_row0 = i * kTileRows;
+    if (!mbar_wait(&full[s], (i / kStages) & 1)) {
+      report(a.err, kErrTimeout, i);
+      break;
+    }
+    const uint8_t* tile = tiles + s * kTileBytes;
+    uint32_t ra[2][8], rb[2][8];
 #pragma unroll
-      for (int m = 0; m < 2; ++m) {
-        const int lr = warp * 32 + m * 16;
-        if (tile_row0 + lr >= rows_total) break;
-        const uint8_t* p = tile + (lr + g) * kRowBytes + 32 * t;
-        const uint4 x0 = *reinterpret_cast<const uint4*>(p);
-        const uint4 x1 = *reinterpret_cast<const uint4*>(p + 16);
-        const uint4 y0 = *reinterpret_cast<const uint4*>(p + 8 * kRowBytes);
-        const uint4 y1 = *reinterpret_cast<const uint4*>(p + 8 * kRowBytes + 16);
-        const uint32_t ra[8] = {x0.x, x0.y, x0.z, x0.w, x1.x, x1.y, x1.z, x1.w};
-        const uint32_t rb[8] = {y0.x, y0.y, y0.z, y0.w, y1.x, y1.y, y1.z, y1.w};
-        float c[4] = {0.f, 0.f, 0.f, 0.f};
+    for (int m = 0; m < 2; ++m) {
+      const uint8_t* p = tile + ((warp * 2 + m) * 16 + g) * kRowBytes + 32 * t;
+      const uint4 x0 = *reinterpret_cast<const uint4*>(p);
+      const uint4 x1 = *reinterpret_cast<const uint4*>(p + 16);
+      const uint4 y0 = *reinterpret_cast<const uint4*>(p + 8 * kRowBytes);
+      const uint4 y1 = *reinterpret_cast<const uint4*>(p + 8 * kRowBytes + 16);
+      ra[m][0] = x0.x; ra[m][1] = x0.y; ra[m][2] = x0.z; ra[m][3] = x0.w;
+      ra[m][4] = x1.x; ra[m][5] = x1.y; ra[m][6] = x1.z; ra[m][7] = x1.w;
+      rb[m][0] = y0.x; rb[m][1] = y0.y; rb[m][2] = y0.z; rb[m][3] = y0.w;
+      rb[m][4] = y1.x; rb[m][5] = y1.y; rb[m][6] = y1.z; rb[m][7] = y1.w;
+    }
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&empty[s]);          // the stage may be refilled
 #pragma unroll
-        for (int ks = 0; ks < 4; ++ks)
-          mma_bf16(c, ra[2 * ks], rb[2 * ks], ra[2 * ks + 1], rb[2 * ks + 1], qf[2 * ks], qf[2 * ks + 1]);
-        // c0, c1: row g, heads 2t, 2t+1;  c2, c3: row g+8, same heads
-        const float h0 = relu ? fmaxf(c[0], 0.f) : c[0];
-        const float h1 = relu ? fmaxf(c[1], 0.f) : c[1];
-        const float h2 = relu ? fmaxf(c[2], 0.f) : c[2];
-        const float h3 = relu ? fmaxf(c[3], 0.f) : c[3];
-        float r0 = __fadd_rn(__fmul_rn(w0, h0), __fmul_rn(w1, h1));
-        float r1 = __fadd_rn(__fmul_rn(w0, h2), __fmul_rn(w1, h3));
-        r0 += __shfl_xor_sync(0xffffffffu, r0, 1);
-        r1 += __shfl_xor_sync(0xffffffffu, r1, 1);
-        r0 += __shfl_xor_sync(0xffffffffu, r0, 2);
-        r1 += __shfl_xor_sync(0xffffffffu, r1, 2);
-        if (t < 2) {
-          const int row = tile_row0 + lr + g + 8 * t;   // local row
-          if (row < rows_total) {
-            const float r = t == 0 ? r0 : r1;
-            if (!POOLED) {
-              const int pos = begin + row;
-              scores[pos] = r;
-              if (cand != nullptr) cand[pos] = pos;
-            } else {
-              const int lp = row / kBlock, tt = row % kBlock;
-              const int blk = s_pool[lp];
-              const int e = blk * kBlock + tt;
-              const int pos = (begin + lp) * kBlock + tt;
-              const bool valid = blk >= 0 && e < nv;
-              scores[pos] = valid ? r : -__int_as_float(0x7f800000);
-              cand[pos] = valid ? e : -1;
-            }
-          }
+    for (int m = 0; m < 2; ++m) {
+      // two independent accumulators (even / odd k-steps) shorten the MMA chain
+      float c0[4] = {0.f, 0.f, 0.f, 0.f}, c1[4] = {0.f, 0.f, 0.f, 0.f};
+      mma_bf16(c0, ra[m][0], rb[m][0], ra[m][1], rb[m][1], qf[0], qf[1]);
+      mma_bf16(c1, ra[m][2], rb[m][2], ra[m][3], rb[m][3], qf[2], qf[3]);
+      mma_bf16(c0, ra[m][4], rb[m][4], ra[m][5], rb[m][5], qf[4], qf[5]);
+      mma_bf16(c1, ra[m][6], rb[m][6], ra[m][7], rb[m][7], qf[6], qf[7]);
+      // c0/c1 [0], [1]: row g, heads 2t, 2t+1;  [2], [3]: row g+8, same heads
+      float h[4];
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const float d = c0[e] + c1[e];
+        h[e] = relu ? fmaxf(d, 0.f) : d;
+      }
+      float r0 = __fadd_rn(__fmul_rn(w0, h[0]), __fmul_rn(w1, h[1]));
+      float r1 = __fadd_rn(__fmul_rn(w0, h[2]), __fmul_rn(w1, h[3]));
+      r0 += __shfl_xor_sync(0xffffffffu, r0, 1);
+      r1 += __shfl_xor_sync(0xffffffffu, r1, 1);
+      r0 += __shfl_xor_sync(0xffffffffu, r0, 2);
+      r1 += __shfl_xor_sync(0xffffffffu, r1, 2);
+      const int row = i * kTileRows + (warp * 2 + m) * 16 + g + 8 * t;   // local row
+      if (t < 2 && row < rows_total) {
+        const float r = t == 0 ? r0 : r1;
+        if (!POOLED) {
+          const int pos = begin + row;
+          scores[pos] = r;
+          if (cand != nullptr) cand[pos] = pos;
+        } else {
+          const int lp = row / kBlock, tt = row % kBlock;
+          const int blk = s_pool[lp];
+          const int e = blk * kBlock + tt;
+          const int pos = (begin + lp) * kBlock + tt;
+          const bool valid = blk >= 0 && e < nv;
+          scores[pos] = valid ? r : -__int_as_float(0x7f800000);
+          cand[pos] = valid ? e : -1;
         }
       }
     }
-    if (!__syncthreads_and(ok)) break;
-    if (tid == 0 && i + kStages < ntiles) issue(i + kStages);
-  }
-  if (i < ntiles && tid == 0) {
-    // A wait gave up: record it and let the copies still in flight land
-    // (bounded again) before the CTA's shared memory is released.
-    report(a.err, kErrTimeout, i);
-    for (int j = i; j < min(i + kStages, ntiles); ++j) mbar_wait(&full[j % kStages], (j / kStages) & 1);
   }
 }
 
@@ -197,6 +216,8 @@ __global__ void __launch_bounds__(kThreads) indexer_mma_kernel(const IndexerArgs
 __global__ void __launch_bounds__(256) indexer_generic_kernel(const IndexerArgs a, int pooled) {
   extern __shared__ float sq[];   // [heads * dim] query, then [heads] weights
   const int b = blockIdx.y;
+  pdl_launch_dependents();
+  pdl_wait();
   const int hd = a.heads * a.dim;
   for (int i = threadIdx.x; i < hd; i += blockDim.x)
     sq[i] = load_elem(a.q_idx, (long long)b * hd + i, a.dtype);
@@ -247,6 +268,8 @@ __global__ void __launch_bounds__(256) indexer_generic_kernel(const IndexerArgs 
 
 __global__ void __launch_bounds__(256) block_keys_kernel(const BlockKeyArgs a) {
   const int b = blockIdx.y;
+  pdl_launch_dependents();
+  pdl_wait();
   const long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x;
   if (i >= (long long)a.nb_cap * a.dim) return;
   const int j = int(i / a.dim), d = int(i % a.dim);
@@ -283,8 +306,7 @@ cudaError_t launch_block_keys(const BlockKeyArgs& a, int batch, cudaStream_t st)
   if (n == 0 || batch == 0) return cudaSuccess;
   dim3 grid(unsigned((n + 255) / 256), unsigned(batch));
   note_launch();
-  block_keys_kernel<<<grid, 256, 0, st>>>(a);
-  return cudaGetLastError();
+  return launch_pdl(block_keys_kernel, grid, dim3(256), 0, st, 1, a);
 }
 
 cudaError_t launch_indexer(const IndexerArgs& in, bool pooled, bool fast, int batch, int max_units,
@@ -297,8 +319,7 @@ cudaError_t launch_indexer(const IndexerArgs& in, bool pooled, bool fast, int ba
     const size_t smem = (size_t(a.heads) * a.dim + a.heads) * sizeof(float);
     dim3 grid(unsigned((positions + 255) / 256), unsigned(batch));
     note_launch();
-    indexer_generic_kernel<<<grid, 256, smem, st>>>(a, pooled ? 1 : 0);
-    return cudaGetLastError();
+    return launch_pdl(indexer_generic_kernel, grid, dim3(256), smem, st, 1, a, pooled ? 1 : 0);
   }
   const size_t smem = fast_smem_bytes(pooled);
   static bool attr_set[2] = {false, false};
@@ -322,8 +343,7 @@ cudaError_t launch_indexer(const IndexerArgs& in, bool pooled, bool fast, int ba
   a.per_cta = per_cta;
   dim3 grid(unsigned((max_units + per_cta - 1) / per_cta), unsigned(batch));
   note_launch();
-  kern<<<grid, kThreads, smem, st>>>(a);
-  return cudaGetLastError();
+  return launch_pdl(kern, grid, dim3(kThreads), smem, st, 1, a);
 }
 
 }  // namespace csa2

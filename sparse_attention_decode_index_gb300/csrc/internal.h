@@ -67,6 +67,31 @@ struct AttnArgs {
   int* err;
 };
 
+// Fused scoring + cluster Top-k (fused.cu): one cluster per query scores its
+// candidates and writes the selected ids (ascending, -1 padded).
+struct SelectArgs {
+  const void* keys;          // [B, rows_per_seq, 64] bf16 (indexer keys or block keys)
+  long long rows_per_seq;
+  const void* q_idx;         // [B, 8, 64] bf16
+  const float* w;            // [B, 8]
+  int relu;
+  const int* n_valid;        // [B]
+  int valid_cap;
+  int div;                   // flat: candidates = ceil(n_valid / div)
+  const int* pool;           // pooled: [B, pool_cap] ascending block ids
+  const int* n_pool;         // pooled: [B]
+  int pool_cap;
+  int rows_per_cta;          // set by the launcher: rows (flat) / pool positions (pooled) per CTA
+  int k;                     // how many to select
+  int* out;                  // [B, ld_out] selected ids
+  long long ld_out;
+  int* n_out;                // [B] number selected (nullable)
+  int* err;
+};
+
+bool index_select_supported(bool pooled, int max_units);
+cudaError_t launch_index_select(const SelectArgs& a, bool pooled, int batch, int max_units, cudaStream_t st);
+
 struct BlockKeyArgs {
   const void* k_idx;         // [B, N, dim]
   const int* n_valid;        // [B]
@@ -76,6 +101,34 @@ struct BlockKeyArgs {
 };
 
 int device_sm_count();
+
+// Launch `kernel` with programmatic stream serialization (PDL) and an optional
+// cluster shape; every kernel of the library calls pdl_wait() before touching
+// data of earlier launches.
+template <typename... Params, typename... Args>
+cudaError_t launch_pdl(void (*kernel)(Params...), dim3 grid, dim3 block, size_t smem, cudaStream_t st,
+                       unsigned cluster_x, Args... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[2];
+  int n = 0;
+  attr[n].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[n].val.programmaticStreamSerializationAllowed = 1;
+  ++n;
+  if (cluster_x > 1) {
+    attr[n].id = cudaLaunchAttributeClusterDimension;
+    attr[n].val.clusterDim.x = cluster_x;
+    attr[n].val.clusterDim.y = 1;
+    attr[n].val.clusterDim.z = 1;
+    ++n;
+  }
+  cfg.attrs = attr;
+  cfg.numAttrs = n;
+  return cudaLaunchKernelEx(&cfg, kernel, args...);
+}
 // Counts kernel launches enqueued by the library (diagnostics: csa2_launch_count).
 void note_launch();
 
@@ -85,6 +138,9 @@ cudaError_t launch_indexer(const IndexerArgs& a, bool pooled, bool fast, int bat
                            cudaStream_t st);
 cudaError_t launch_topk(const TopkArgs& a, int chunks, int batch, cudaStream_t st);
 int topk_max_chunk();
+// Cluster Top-k over one row of up to topk_cluster_max() positions (one launch).
+cudaError_t launch_topk_cluster(const TopkArgs& a, int batch, cudaStream_t st);
+int topk_cluster_max();
 int attn_max_cluster();
 int attn_slots_per_cta();
 // fast: bf16, 64 heads, dk 192, dv 128
