@@ -184,6 +184,29 @@ int csa2_layer_group(const csa2_shape* shape, const csa2_layer* layers, int32_t 
                      const int32_t* n_valid, const int32_t* n_swa, void* ws, size_t ws_bytes,
                      csa2_stream_t stream);
 
+/* csa2_layer_group for callers that cannot allocate device memory -- the
+ * paper has no counterpart; this is a convenience of this library.  Some
+ * callers have no way to provide a workspace: a plugin inside a host framework
+ * that owns all device memory and exposes no allocator, or a latency-critical
+ * decode loop that must not call cudaMalloc (it can synchronise the device).
+ * This entry point takes the same arguments as csa2_layer_group minus the
+ * workspace, and runs the same layer group on a 32 MiB scratch array that the
+ * library holds in device memory (a file-scope __device__ array: every GPU
+ * that loads the library keeps it until the process exits).
+ *   - Shapes whose csa2_workspace_bytes exceeds 32 MiB return
+ *     CSA2_ERR_WORKSPACE and enqueue nothing.
+ *   - The first call made while a device is current looks up the array's
+ *     device address and zeroes its header (the sticky device error word) on
+ *     `stream`; make that first call before any stream capture.
+ *   - Every call shares the one array: calls that may overlap on the GPU (on
+ *     different streams, or from different host threads without ordering)
+ *     race on it and must be serialised by the caller.
+ *   - No memory is allocated or freed; device-side range problems are still
+ *     skipped by the kernels as in csa2_layer_group. */
+int csa2_layer_group_static(const csa2_shape* shape, const csa2_layer* layers, int32_t n_layers,
+                            const void* k_main, const void* v_main, const void* k_idx, const void* kb,
+                            const int32_t* n_valid, const int32_t* n_swa, csa2_stream_t stream);
+
 /* Static description of a status code. */
 const char* csa2_status_str(int status);
 

@@ -64,6 +64,8 @@ _SIGS = {
     "csa2_read_device_error": (ctypes.c_int, [_VP, _VP, ctypes.POINTER(_I32)]),
     "csa2_fast_path": (ctypes.c_int, [ctypes.POINTER(CShape), ctypes.POINTER(_I32), ctypes.POINTER(_I32)]),
     "csa2_launch_count": (ctypes.c_ulonglong, []),
+    "csa2_layer_group_static": (ctypes.c_int, [ctypes.POINTER(CShape), ctypes.POINTER(CLayer), _I32, _VP, _VP,
+                                               _VP, _VP, _VP, _VP, _VP]),
 }
 
 
@@ -237,6 +239,23 @@ class LayerGroupCall:
 
 def layer_group(shape, layers, k_main, v_main, k_idx, kb, n_valid, n_swa, ws, stream=None):
     LayerGroupCall(shape, layers, k_main, v_main, k_idx, kb, n_valid, n_swa, ws)(stream)
+
+
+def layer_group_static(shape, layers, k_main, v_main, k_idx, kb, n_valid, n_swa, stream=None):
+    """csa2_layer_group on the library's own 32 MiB device scratch (no workspace argument).
+
+    For callers that cannot allocate device memory (a plugin whose host
+    framework owns all allocations, or a decode loop that must not call
+    cudaMalloc).  Calls share the scratch, so calls that may overlap on the
+    GPU must be serialised by the caller."""
+    e = elem_dtype(shape)
+    s = c_shape(shape)
+    ls = [_layer(L, e) for L in layers]
+    arr = (CLayer * len(ls))(*ls)
+    _check(lib().csa2_layer_group_static(ctypes.byref(s), arr, len(ls), _ptr(k_main, e, "k_main"),
+                                         _ptr(v_main, e, "v_main"), _ptr(k_idx, e, "k_idx"), _ptr(kb, e, "kb"),
+                                         _ptr(n_valid, torch.int32, "n_valid"), _ptr(n_swa, torch.int32, "n_swa"),
+                                         _stream(stream)), "csa2_layer_group_static")
 
 
 def read_device_error(ws, stream=None):
