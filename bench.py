@@ -428,6 +428,31 @@ def run_ours(args):
     return 0
 
 
+def profiled_traffic(wl, hier: bool):
+    """DRAM bytes per launch of the fused pooled kernel from the committed ncu summary, or None
+    when no summary covers this workload or the kernel source changed since it was captured."""
+    import hashlib
+    if not hier or wl.name != "reindex_b64_128k":
+        return None, "no ncu capture of this workload's kernel"
+    prof = os.path.join(ROOT, "profiles", "index_select_pooled__reindex_b64_128k.md")
+    if not os.path.exists(prof):
+        return None, "no ncu summary"
+    fields = {}
+    with open(prof) as f:
+        for line in f:
+            if ":" in line and line.split(":")[0].strip() in ("dram_bytes_per_launch", "source_sha256_16"):
+                k, v = line.split(":", 1)
+                fields[k.strip()] = v.strip()
+    h = hashlib.sha256()
+    for name in ("fused.cu", "common.cuh", "internal.h"):
+        with open(os.path.join(ROOT, "sparse_attention_decode_index_gb300", "csrc", name), "rb") as f:
+            h.update(f.read())
+    if fields.get("source_sha256_16") != h.hexdigest()[:16]:
+        return None, "kernel source changed since the ncu capture"
+    return int(fields["dram_bytes_per_launch"]), "dram__bytes_read.sum + dram__bytes_write.sum, " + \
+        "profiles/index_select_pooled__reindex_b64_128k.md"
+
+
 def dominant_kernel_roofline(csa2, wl, d, stream, flush, args, peak, peak_src):
     """Time the step's dominant kernel alone (CUDA events on its stream, L2 flushed between launches)."""
     import torch
@@ -435,10 +460,8 @@ def dominant_kernel_roofline(csa2, wl, d, stream, flush, args, peak, peak_src):
     L0 = next(L for L in d["layers"] if L["mode"] != W.REUSE)
     hier = bool(L0.get("hier"))
     dev = d["k_idx"].device
-    scores = torch.empty((sh.batch, max(sh.n_entries, sh.pool_blocks * sh.block)), dtype=torch.float32, device=dev)
-    cand = torch.empty_like(scores, dtype=torch.int32)
-    n_cand = torch.empty(sh.batch, dtype=torch.int32, device=dev)
     reps = max(args.steps, 10)
+    idx = torch.empty((sh.batch, sh.topk), dtype=torch.int32, device=dev)
     with torch.cuda.stream(stream):
         if hier:
             pool = torch.empty((sh.batch, sh.pool_blocks), dtype=torch.int32, device=dev)
@@ -446,15 +469,16 @@ def dominant_kernel_roofline(csa2, wl, d, stream, flush, args, peak, peak_src):
             csa2.index_blocks(sh, L0["q_idx"], L0["w_idx"], d["kb"], d["n_valid"], pool, n_pool, d["ws"], stream)
 
             def launch():
-                csa2.index_tokens(sh, L0["q_idx"], L0["w_idx"], d["k_idx"], d["n_valid"], scores, d["ws"],
-                                  pool=pool, n_pool=n_pool, cand_out=cand, n_cand_out=n_cand, stream=stream)
-            name = "indexer_mma_kernel<pooled> (csa2_index_tokens over the 2,048-block pool)"
+                csa2.index_topk(sh, L0["q_idx"], L0["w_idx"], d["k_idx"], d["n_valid"], sh.topk, idx, d["ws"],
+                                pool=pool, n_pool=n_pool, stream=stream)
+            name = ("index_select_kernel<pooled> (csa2_index_topk: pooled token scoring + exact Top-512, "
+                    "one cluster per query)")
             n_rows = sum(min(sh.pool_blocks, -(-int(v) // sh.block)) * sh.block for v in wl.n_valid)
         else:
             def launch():
-                csa2.index_tokens(sh, L0["q_idx"], L0["w_idx"], d["k_idx"], d["n_valid"], scores, d["ws"],
-                                  n_cand_out=n_cand, stream=stream)
-            name = "indexer_mma_kernel<flat> (csa2_index_tokens over every entry)"
+                csa2.index_topk(sh, L0["q_idx"], L0["w_idx"], d["k_idx"], d["n_valid"], sh.topk, idx, d["ws"],
+                                stream=stream)
+            name = "index_select_kernel<flat> (csa2_index_topk: flat token scoring + exact Top-512)"
             n_rows = int(sum(int(v) for v in wl.n_valid))
         launch()
         torch.cuda.synchronize()
@@ -471,8 +495,10 @@ def dominant_kernel_roofline(csa2, wl, d, stream, flush, args, peak, peak_src):
     alg = n_rows * sh.idx_dim * e
     avg = sum(ms) / len(ms)
     gbs = alg / (avg / 1e3) / 1e9
+    traffic, traffic_src = profiled_traffic(wl, hier)
     return {"bound": "hbm", "kernel": name, "achieved": gbs, "peak": peak, "unit": "GB/s", "frac": gbs / peak,
-            "traffic": None, "alg_bytes_per_launch": alg, "launch_us": 1e3 * avg, "peak_source": peak_src,
+            "traffic": traffic, "traffic_source": traffic_src, "alg_bytes_per_launch": alg, "launch_us": 1e3 * avg,
+            "peak_source": peak_src,
             "timing": f"alone, {reps} launches, CUDA events on its stream, L2 flushed before each"}
 
 

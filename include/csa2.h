@@ -148,6 +148,23 @@ int csa2_index_tokens(const csa2_shape* shape, const void* q_idx, const float* w
                       float* scores_out, int32_t* cand_out, int32_t* n_cand_out, void* ws,
                       size_t ws_bytes, csa2_stream_t stream);
 
+/* Token scoring and exact Top-k in one call: the candidates of
+ * csa2_index_tokens (flat when pool == NULL, else the pooled blocks' entries)
+ * are scored and the top k (1 <= k <= shape.topk) selected under (score
+ * descending, entry index ascending), as csa2_index_tokens followed by
+ * csa2_topk would -- bullet "Sparse attention" (Top-512) and bullet
+ * "Hierarchical indexer" (at most 16,384 pooled candidates).  On the fast
+ * path (bf16, 8 x 64 indexer, blocks of 8) one thread-block cluster per query
+ * scores its candidates and selects in shared memory without writing scores
+ * to HBM.
+ *   q_idx [B, HI, dI]  w [B, HI]  k_idx [B, N, dI]  n_valid [B]
+ *   pool [B, P], n_pool [B] (from csa2_index_blocks) or NULL
+ *   idx_out [B, k] (output) selected entry ids ascending, padded with -1
+ *   n_out   [B]    (output, nullable) number selected */
+int csa2_index_topk(const csa2_shape* shape, const void* q_idx, const float* w, const void* k_idx,
+                    const int32_t* n_valid, const int32_t* pool, const int32_t* n_pool, int32_t k,
+                    int32_t* idx_out, int32_t* n_out, void* ws, size_t ws_bytes, csa2_stream_t stream);
+
 /* Exact Top-k of each row: scores [B, ld] (row stride ld), optional candidate
  * ids cand [B, ld] (NULL: the id is the position; ids < 0 are skipped; ids
  * must ascend with position), n_cand [B] positions to consider (NULL: ld).

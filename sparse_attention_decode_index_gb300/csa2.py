@@ -55,6 +55,8 @@ _SIGS = {
     "csa2_index_blocks": (ctypes.c_int, [ctypes.POINTER(CShape), _VP, _VP, _VP, _VP, _VP, _VP, _VP, _SZ, _VP]),
     "csa2_index_tokens": (ctypes.c_int, [ctypes.POINTER(CShape), _VP, _VP, _VP, _VP, _VP, _VP, _VP, _VP, _VP,
                                          _VP, _SZ, _VP]),
+    "csa2_index_topk": (ctypes.c_int, [ctypes.POINTER(CShape), _VP, _VP, _VP, _VP, _VP, _VP, _I32, _VP, _VP, _VP,
+                                       _SZ, _VP]),
     "csa2_topk": (ctypes.c_int, [ctypes.POINTER(CShape), _VP, _I32, _VP, _VP, _I32, _VP, _VP, _VP, _SZ, _VP]),
     "csa2_sparse_attn": (ctypes.c_int, [ctypes.POINTER(CShape), _VP, _VP, _VP, _VP, _VP, _VP, _VP, _VP, _VP,
                                         _VP, _SZ, _VP]),
@@ -188,6 +190,18 @@ def index_tokens(shape, q_idx, w, k_idx, n_valid, scores_out, ws, pool=None, n_p
                                    _ptr(cand_out, torch.int32, "cand_out"),
                                    _ptr(n_cand_out, torch.int32, "n_cand_out"), _ptr(ws, torch.uint8, "ws"),
                                    ws.numel(), _stream(stream)), "csa2_index_tokens")
+
+
+def index_topk(shape, q_idx, w, k_idx, n_valid, k: int, idx_out, ws, pool=None, n_pool=None, n_out=None,
+               stream=None):
+    """Score the candidates (flat, or the pooled blocks' entries) and select the Top-k in one call."""
+    s = c_shape(shape)
+    e = elem_dtype(shape)
+    _check(lib().csa2_index_topk(ctypes.byref(s), _ptr(q_idx, e, "q_idx"), _ptr(w, torch.float32, "w"),
+                                 _ptr(k_idx, e, "k_idx"), _ptr(n_valid, torch.int32, "n_valid"),
+                                 _ptr(pool, torch.int32, "pool"), _ptr(n_pool, torch.int32, "n_pool"), int(k),
+                                 _ptr(idx_out, torch.int32, "idx_out"), _ptr(n_out, torch.int32, "n_out"),
+                                 _ptr(ws, torch.uint8, "ws"), ws.numel(), _stream(stream)), "csa2_index_topk")
 
 
 def topk(shape, scores, k: int, idx_out, ws, cand=None, n_cand=None, score_out=None, stream=None):

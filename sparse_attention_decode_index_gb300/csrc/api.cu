@@ -366,6 +366,42 @@ int csa2_index_tokens(const csa2_shape* shape, const void* q_idx, const float* w
                          stream);
 }
 
+int csa2_index_topk(const csa2_shape* shape, const void* q_idx, const float* w, const void* k_idx,
+                    const int32_t* n_valid, const int32_t* pool, const int32_t* n_pool, int32_t k, int32_t* idx_out,
+                    int32_t* n_out, void* ws, size_t ws_bytes, csa2_stream_t stream) {
+  CSA2_TRY(check_shape(shape));
+  const csa2_shape& s = *shape;
+  CSA2_TRY(check_ws(s, ws, ws_bytes));
+  if (q_idx == nullptr || w == nullptr || k_idx == nullptr || n_valid == nullptr || idx_out == nullptr || k < 1)
+    return CSA2_ERR_INVALID_ARG;
+  if (k > s.topk) return CSA2_ERR_INVALID_ARG;      // the workspace is sized for shape.topk
+  if (indexer_fast(s) && !aligned16(k_idx)) return CSA2_ERR_INVALID_ARG;
+  const WsLayout L = layout(s);
+  int* err = at<int>(ws, L.hdr);
+  float* ts = at<float>(ws, L.tok_scores);
+  int32_t* tc = at<int32_t>(ws, L.tok_cand);
+  int32_t* nc = at<int32_t>(ws, L.n_cand);
+  if (pool == nullptr) {
+    if (indexer_fast(s) && index_select_supported(false, s.n_entries)) {
+      SelectArgs a = select_args(s, k_idx, s.n_entries, q_idx, w, n_valid, 1, k, idx_out, k, n_out, err);
+      return cuda_status(launch_index_select(a, false, s.batch, s.n_entries, stream));
+    }
+    CSA2_TRY(do_index_flat(s, q_idx, w, k_idx, s.n_entries, n_valid, 1, ts, nullptr, nc, s.n_entries, err, stream));
+    return do_topk(s, L, ws, ts, s.n_entries, nullptr, nc, s.n_entries, k, idx_out, nullptr, n_out, stream);
+  }
+  if (s.pool_blocks < 1 || n_pool == nullptr || s.n_entries % s.block != 0) return CSA2_ERR_INVALID_ARG;
+  if (pooled_fast(s) && index_select_supported(true, s.pool_blocks)) {
+    SelectArgs a = select_args(s, k_idx, s.n_entries, q_idx, w, n_valid, 1, k, idx_out, k, n_out, err);
+    a.pool = pool;
+    a.n_pool = n_pool;
+    a.pool_cap = s.pool_blocks;
+    return cuda_status(launch_index_select(a, true, s.batch, s.pool_blocks, stream));
+  }
+  CSA2_TRY(do_index_pooled(s, q_idx, w, k_idx, n_valid, pool, n_pool, ts, tc, nc, err, stream));
+  const int64_t ld = int64_t(s.pool_blocks) * s.block;
+  return do_topk(s, L, ws, ts, ld, tc, nc, ld, k, idx_out, nullptr, n_out, stream);
+}
+
 int csa2_topk(const csa2_shape* shape, const float* scores, int32_t ld, const int32_t* cand,
               const int32_t* n_cand, int32_t k, int32_t* idx_out, float* score_out, void* ws, size_t ws_bytes,
               csa2_stream_t stream) {

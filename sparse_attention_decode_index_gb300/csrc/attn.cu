@@ -10,15 +10,20 @@
 // ceil(slots / 160) CTAs (4 for the architecture's 640 slots), sized so that two
 // CTAs fit per SM and every cluster of a 64-query batch is resident in one wave.
 // Each CTA gathers its 160 K rows (384 B) and V rows (256 B) into padded
-// shared-memory rows with one bulk (TMA) copy per row, all completing on one
-// mbarrier; invalid slots (index -1, or beyond n_swa) are zero-filled and
-// masked.  Four warps each own 16 heads; their Q fragments are loaded straight
+// shared-memory rows with 16-byte cp.async copies -- consecutive threads copy
+// consecutive 16-byte pieces of one row, so every row is read contiguously --
+// in two commit groups (slots 0..79, 80..159) so the first half of the keys
+// can be scored while the second is still arriving.  (Per-row bulk copies were
+// measured to be limited by the rate at which the TMA unit accepts small
+// copies.)  Invalid slots (index -1, or beyond n_swa) are zero-filled by the
+// copies themselves and masked.  Four warps each own 16 heads; their Q fragments are loaded straight
 // into registers while the gather is in flight.  S = Q K^T and O = P V run on
 // mma.sync m16n8k16 (bf16 in, fp32 accumulate) with a base-2 fp32 softmax.
-// The partial (m, l, O) of every CTA is merged in fixed CTA order through
-// distributed shared memory: per-head factors exp2(m_c - M) / L first, then
-// 16-byte remote loads of the partial O rows.  No partial touches global
-// memory and the result is deterministic.
+// The partials of the cluster are merged through distributed shared memory
+// with remote stores only: every CTA writes its per-head (m, l) into every
+// CTA, scales its own partial O by exp2(m_c - M) / L and pushes it to the CTA
+// that owns those heads, which sums the pushed partials in fixed CTA order.
+// No partial touches global memory and the result is deterministic.
 #include "common.cuh"
 #include "internal.h"
 
@@ -37,23 +42,16 @@ constexpr int kMaxCluster = 8;
 
 constexpr int kOffK = 0;
 constexpr int kOffV = kOffK + kSlots * kKRow;     // 64,000
-constexpr int kOffM = kOffV + kSlots * kVRow;     // 107,520
-constexpr int kOffL = kOffM + kH * 4;
-constexpr int kOffF = kOffL + kH * 4;             // [kMaxCluster][kH] merge factors
-constexpr int kOffValid = kOffF + kMaxCluster * kH * 4;
-constexpr int kOffBar = kOffValid + kSlots * 4;
-constexpr int kSmemBytes = kOffBar + 2 * 8;
+constexpr int kOffM = kOffV + kSlots * kVRow;     // 107,520: [kMaxCluster][kH] m of every CTA
+constexpr int kOffL = kOffM + kMaxCluster * kH * 4;   // [kMaxCluster][kH] l of every CTA
+constexpr int kOffValid = kOffL + kMaxCluster * kH * 4;
+constexpr int kOffSrc = kOffValid + kSlots * 4;            // [kSlots] K row, then [kSlots] V row addresses
+constexpr int kSmemBytes = kOffSrc + 2 * kSlots * 8;
 constexpr int kHalf = kSlots / 2;                 // slots per gather barrier (80)
-static_assert(kH * kORow * 4 <= kSlots * kKRow, "partial O must fit in the K region");
+// pushed partials: [ncta][ceil(kH / ncta)][kDv] floats in the (dead) K region
+static_assert((kH + kMaxCluster - 1) * kDv * 4 <= kSlots * kKRow, "pushed partials must fit in the K region");
 static_assert(kSlots % 16 == 0, "PV k-steps need 16-key groups");
 static_assert(kNT % 4 == 0, "each gather half covers whole n-tile pairs");
-
-CSA2_DEV void dsmem_ld_v4(float4& v, uint32_t addr) {
-  asm volatile("ld.shared::cluster.v4.f32 {%0,%1,%2,%3}, [%4];"
-               : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
-               : "r"(addr)
-               : "memory");
-}
 
 __global__ void __launch_bounds__(kThreads, 2) attn_mma_kernel(const AttnArgs a) {
   extern __shared__ __align__(128) uint8_t smem[];
@@ -61,10 +59,10 @@ __global__ void __launch_bounds__(kThreads, 2) attn_mma_kernel(const AttnArgs a)
   uint8_t* sV = smem + kOffV;
   float* sM = reinterpret_cast<float*>(smem + kOffM);
   float* sL = reinterpret_cast<float*>(smem + kOffL);
-  float* sF = reinterpret_cast<float*>(smem + kOffF);
   int* sValid = reinterpret_cast<int*>(smem + kOffValid);
-  uint64_t* bar = reinterpret_cast<uint64_t*>(smem + kOffBar);
-  float* sO = reinterpret_cast<float*>(smem + kOffK);   // reused after S = QK^T
+  const uint8_t** sKsrc = reinterpret_cast<const uint8_t**>(smem + kOffSrc);
+  const uint8_t** sVsrc = sKsrc + kSlots;
+  float* sRecv = reinterpret_cast<float*>(smem + kOffK);   // pushed partials, after S and PV everywhere
 
   const int b = blockIdx.y;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -72,11 +70,6 @@ __global__ void __launch_bounds__(kThreads, 2) attn_mma_kernel(const AttnArgs a)
   const uint32_t crank = cluster_rank(), ncta = cluster_size();
 
   pdl_launch_dependents();
-  if (tid == 0) {
-    mbar_init(&bar[0], kThreads);
-    mbar_init(&bar[1], kThreads);
-    mbar_fence_init();
-  }
   // --- Q A-fragments for heads 16w + g and 16w + g + 8, straight from global
   uint32_t qa[kDk / 16][4];
   {
@@ -92,71 +85,63 @@ __global__ void __launch_bounds__(kThreads, 2) attn_mma_kernel(const AttnArgs a)
     }
   }
   pdl_wait();   // the indices come from the preceding launch
-  __syncthreads();
 
-  // --- gather: thread `tid` owns key slots tid and tid + 128 of this CTA; slots
-  // [0, 80) complete on bar[0] and [80, 160) on bar[1], so the first half can be
-  // scored while the second is still arriving
-  uint32_t tx0 = 0u, tx1 = 0u;
-  const uint8_t* ksrc[2] = {nullptr, nullptr};
-  const uint8_t* vsrc[2] = {nullptr, nullptr};
+  // --- source rows of this CTA's 160 key slots (null: invalid slot)
   const int ns = clamp_count(a.n_swa[b], a.swa, a.err);
-#pragma unroll
-  for (int j = 0; j < 2; ++j) {
-    const int ls = tid + j * kThreads;
-    if (ls >= kSlots) break;
+  for (int ls = tid; ls < kSlots; ls += kThreads) {
     const int slot = blockIdx.x * kSlots + ls;
+    const uint8_t* ks = nullptr;
+    const uint8_t* vs = nullptr;
     if (slot < a.topk) {
       const int e = a.idx[(long long)b * a.topk + slot];
       if (e >= a.n_entries) report(a.err, kErrBadIndex, e);
       if (e >= 0 && e < a.n_entries) {
         const long long r = (long long)b * a.n_entries + e;
-        ksrc[j] = static_cast<const uint8_t*>(a.k_main) + r * (kDk * 2);
-        vsrc[j] = static_cast<const uint8_t*>(a.v_main) + r * (kDv * 2);
+        ks = static_cast<const uint8_t*>(a.k_main) + r * (kDk * 2);
+        vs = static_cast<const uint8_t*>(a.v_main) + r * (kDv * 2);
       }
     } else if (slot < a.topk + a.swa && slot - a.topk < ns) {
       const long long r = (long long)b * a.swa + (slot - a.topk);
-      ksrc[j] = static_cast<const uint8_t*>(a.k_swa) + r * (kDk * 2);
-      vsrc[j] = static_cast<const uint8_t*>(a.v_swa) + r * (kDv * 2);
+      ks = static_cast<const uint8_t*>(a.k_swa) + r * (kDk * 2);
+      vs = static_cast<const uint8_t*>(a.v_swa) + r * (kDv * 2);
     }
-    sValid[ls] = ksrc[j] != nullptr ? 1 : 0;
-    if (ksrc[j] != nullptr) {
-      if (ls < kHalf)
-        tx0 += kDk * 2 + kDv * 2;
-      else
-        tx1 += kDk * 2 + kDv * 2;
-    }
+    sKsrc[ls] = ks;
+    sVsrc[ls] = vs;
+    sValid[ls] = ks != nullptr ? 1 : 0;
   }
-  mbar_arrive_expect_tx(&bar[0], tx0);
-  mbar_arrive_expect_tx(&bar[1], tx1);
-#pragma unroll
-  for (int j = 0; j < 2; ++j) {
-    const int ls = tid + j * kThreads;
-    if (ls >= kSlots) break;
-    uint64_t* hb = &bar[ls < kHalf ? 0 : 1];
-    if (ksrc[j] != nullptr) {
-      bulk_g2s(sK + ls * kKRow, ksrc[j], kDk * 2, hb);
-      bulk_g2s(sV + ls * kVRow, vsrc[j], kDv * 2, hb);
-    } else {
-      const uint4 z = make_uint4(0u, 0u, 0u, 0u);
-      for (int i = 0; i < kDk * 2; i += 16) *reinterpret_cast<uint4*>(sK + ls * kKRow + i) = z;
-      for (int i = 0; i < kDv * 2; i += 16) *reinterpret_cast<uint4*>(sV + ls * kVRow + i) = z;
-    }
-  }
-  __syncthreads();   // zero-filled rows and slot flags visible to every warp
+  __syncthreads();
 
-  // --- S = Q K^T for heads [16w, 16w + 16) x 160 keys, one half per gather barrier
+  // --- gather: 16-byte pieces, 24 per K row and 16 per V row; two commit groups
+  constexpr int kPieces = (kDk * 2 + kDv * 2) / 16;        // 40 per slot
+  const uint8_t* zsrc = static_cast<const uint8_t*>(a.k_main);   // any valid address (0 bytes read)
+#pragma unroll
+  for (int half = 0; half < 2; ++half) {
+    for (int c = tid; c < kHalf * kPieces; c += kThreads) {
+      const int ls = half * kHalf + c / kPieces, part = c % kPieces;
+      const bool isk = part < (kDk * 2) / 16;
+      const uint8_t* row = isk ? sKsrc[ls] : sVsrc[ls];
+      const int off = isk ? part * 16 : (part - (kDk * 2) / 16) * 16;
+      uint8_t* dst = isk ? sK + ls * kKRow + off : sV + ls * kVRow + off;
+      const uint32_t n = row != nullptr ? 16u : 0u;          // 0 source bytes: zero fill
+      asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(smem_u32(dst)),
+                   "l"(row != nullptr ? row + off : zsrc), "r"(n)
+                   : "memory");
+    }
+    asm volatile("cp.async.commit_group;" ::: "memory");
+  }
+
+  // --- S = Q K^T for heads [16w, 16w + 16) x 160 keys, one half per commit group
   float s[kNT][4];
 #pragma unroll
   for (int j = 0; j < kNT; ++j) s[j][0] = s[j][1] = s[j][2] = s[j][3] = 0.f;
   const uint8_t* krow = sK + ((lane & 7) + 8 * (lane >> 4)) * kKRow + ((lane >> 3) & 1) * 16;
 #pragma unroll
   for (int half = 0; half < 2; ++half) {
-    if (!mbar_wait(&bar[half], 0)) {
-      // record the stall, give the copies in flight one more bounded wait
-      report(a.err, kErrTimeout, b);
-      mbar_wait(&bar[half], 0);
-    }
+    if (half == 0)
+      asm volatile("cp.async.wait_group 1;" ::: "memory");
+    else
+      asm volatile("cp.async.wait_group 0;" ::: "memory");
+    __syncthreads();
 #pragma unroll
     for (int ks = 0; ks < kDk / 16; ++ks) {
 #pragma unroll
@@ -223,86 +208,70 @@ __global__ void __launch_bounds__(kThreads, 2) attn_mma_kernel(const AttnArgs a)
     }
   }
 
-  // --- partial (m, l, O) of this CTA into shared memory (O over the K region)
-  __syncthreads();
+  // --- merge across the cluster (remote stores only)
   const int h0 = warp * 16 + g, h1 = h0 + 8;
-#pragma unroll
-  for (int j = 0; j < kDv / 8; ++j) {
-    *reinterpret_cast<float2*>(sO + h0 * kORow + 8 * j + 2 * t) = make_float2(o[j][0], o[j][1]);
-    *reinterpret_cast<float2*>(sO + h1 * kORow + 8 * j + 2 * t) = make_float2(o[j][2], o[j][3]);
-  }
+  // 1. every CTA's (m, l) of every head into every CTA: table [rank][head]
   if (t == 0) {
-    sM[h0] = m0;
-    sL[h0] = l0;
-    sM[h1] = m1;
-    sL[h1] = l1;
-  }
-  cluster_sync_all();
-
-  // --- merge factors f_c[h] = exp2(m_c - M) / L for every CTA c (fixed order);
-  // all remote loads are issued before any of them is used
-  if (tid < kH) {
-    const int h = tid;
-    float mr[kMaxCluster], lr[kMaxCluster];
-#pragma unroll
-    for (int r = 0; r < kMaxCluster; ++r) {
-      if (r < int(ncta)) {
-        mr[r] = dsmem_ld_f32(dsmem_addr(sM + h, r));
-        lr[r] = dsmem_ld_f32(dsmem_addr(sL + h, r));
-      } else {
-        mr[r] = -INFINITY;
-        lr[r] = 0.f;
-      }
+    for (uint32_t r = 0; r < ncta; ++r) {
+      dsmem_st_f32(dsmem_addr(sM + crank * kH + h0, r), m0);
+      dsmem_st_f32(dsmem_addr(sL + crank * kH + h0, r), l0);
+      dsmem_st_f32(dsmem_addr(sM + crank * kH + h1, r), m1);
+      dsmem_st_f32(dsmem_addr(sL + crank * kH + h1, r), l1);
     }
+  }
+  cluster_sync_all();   // tables complete; every CTA is past its S and PV (K/V regions free)
+  // 2. own factor exp2(m_own - M) / L for rows h0, h1; scale and push to the head's owner
+  const int per_owner = (kH + int(ncta) - 1) / int(ncta);
+  float f0 = 0.f, f1 = 0.f;
+  {
+    float M0 = -INFINITY, M1 = -INFINITY;
+    for (uint32_t r = 0; r < ncta; ++r) {
+      M0 = fmaxf(M0, sM[r * kH + h0]);
+      M1 = fmaxf(M1, sM[r * kH + h1]);
+    }
+    float L0 = 0.f, L1 = 0.f;
+    for (uint32_t r = 0; r < ncta; ++r) {
+      const float a0 = sM[r * kH + h0], a1 = sM[r * kH + h1];
+      if (a0 != -INFINITY) L0 += exp2f(a0 - M0) * sL[r * kH + h0];
+      if (a1 != -INFINITY) L1 += exp2f(a1 - M1) * sL[r * kH + h1];
+    }
+    if (M0 != -INFINITY && m0 != -INFINITY) f0 = exp2f(m0 - M0) / L0;
+    if (M1 != -INFINITY && m1 != -INFINITY) f1 = exp2f(m1 - M1) / L1;
+  }
+  {
+    const uint32_t own0 = uint32_t(h0 / per_owner), own1 = uint32_t(h1 / per_owner);
+    float* dst0 = sRecv + ((size_t)crank * per_owner + (h0 - int(own0) * per_owner)) * kDv;
+    float* dst1 = sRecv + ((size_t)crank * per_owner + (h1 - int(own1) * per_owner)) * kDv;
+#pragma unroll
+    for (int j = 0; j < kDv / 8; ++j) {
+      dsmem_st_v2(dsmem_addr(dst0 + 8 * j + 2 * t, own0), o[j][0] * f0, o[j][1] * f0);
+      dsmem_st_v2(dsmem_addr(dst1 + 8 * j + 2 * t, own1), o[j][2] * f1, o[j][3] * f1);
+    }
+  }
+  cluster_sync_all();   // every pushed partial has landed in its owner
+  // 3. the owner sums its heads in CTA order and writes out / lse
+  const int hb = int(crank) * per_owner, he = min(kH, hb + per_owner);
+  for (int e = tid; e < (he - hb) * (kDv / 4); e += kThreads) {
+    const int hl = e / (kDv / 4), d4 = e % (kDv / 4);
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (uint32_t r = 0; r < ncta; ++r) {
+      const float4 v = *reinterpret_cast<const float4*>(sRecv + ((size_t)r * per_owner + hl) * kDv + 4 * d4);
+      acc.x += v.x;
+      acc.y += v.y;
+      acc.z += v.z;
+      acc.w += v.w;
+    }
+    *reinterpret_cast<float4*>(a.out + ((long long)b * kH + hb + hl) * kDv + 4 * d4) = acc;
+  }
+  if (a.lse != nullptr && tid < he - hb) {
+    const int h = hb + tid;
     float M = -INFINITY;
-#pragma unroll
-    for (int r = 0; r < kMaxCluster; ++r) M = fmaxf(M, mr[r]);
+    for (uint32_t r = 0; r < ncta; ++r) M = fmaxf(M, sM[r * kH + h]);
     float L = 0.f;
-#pragma unroll
-    for (int r = 0; r < kMaxCluster; ++r)
-      if (mr[r] != -INFINITY) L += exp2f(mr[r] - M) * lr[r];
-#pragma unroll
-    for (int r = 0; r < kMaxCluster; ++r)
-      if (r < int(ncta)) sF[r * kH + h] = (M == -INFINITY || mr[r] == -INFINITY) ? 0.f : exp2f(mr[r] - M) / L;
-    if (crank == 0 && a.lse != nullptr)
-      a.lse[(long long)b * kH + h] = M == -INFINITY ? -INFINITY : (M + log2f(L)) * 0.6931471805599453f;
+    for (uint32_t r = 0; r < ncta; ++r)
+      if (sM[r * kH + h] != -INFINITY) L += exp2f(sM[r * kH + h] - M) * sL[r * kH + h];
+    a.lse[(long long)b * kH + h] = M == -INFINITY ? -INFINITY : (M + log2f(L)) * 0.6931471805599453f;
   }
-  __syncthreads();
-
-  // --- out[h, 4d..4d+4) = sum_c f_c[h] * O_c[h, 4d..4d+4); thread owns float4 slices.
-  // The cluster has ncta * 128 threads and 64 * 32 slices: with ncta = 4 every
-  // thread owns exactly 4 slices; all their remote loads are issued up front.
-  constexpr int kSlices = kH * kDv / 4;
-  const int nthreads = int(ncta) * kThreads;
-  for (int e0 = int(crank) * kThreads + tid; e0 < kSlices; e0 += 4 * nthreads) {
-    float4 v[4][kMaxCluster];
-#pragma unroll
-    for (int u = 0; u < 4; ++u) {
-      const int e = e0 + u * nthreads;
-      const int h = e / (kDv / 4), d4 = e % (kDv / 4);
-#pragma unroll
-      for (int r = 0; r < kMaxCluster; ++r)
-        if (e < kSlices && r < int(ncta)) dsmem_ld_v4(v[u][r], dsmem_addr(sO + h * kORow + 4 * d4, r));
-    }
-#pragma unroll
-    for (int u = 0; u < 4; ++u) {
-      const int e = e0 + u * nthreads;
-      if (e >= kSlices) break;
-      const int h = e / (kDv / 4), d4 = e % (kDv / 4);
-      float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll
-      for (int r = 0; r < kMaxCluster; ++r) {
-        if (r >= int(ncta)) break;
-        const float f = sF[r * kH + h];
-        acc.x += f * v[u][r].x;
-        acc.y += f * v[u][r].y;
-        acc.z += f * v[u][r].z;
-        acc.w += f * v[u][r].w;
-      }
-      *reinterpret_cast<float4*>(a.out + ((long long)b * kH + h) * kDv + 4 * d4) = acc;
-    }
-  }
-  cluster_sync_all();
 }
 
 // Generic path: any head count / dims / element type; one CTA per (query, head).

@@ -267,3 +267,43 @@ def test_sparse_attn_flags_out_of_range_index(csa2):
     ref, _ = oracle.sparse_attention(oracle.to_f64(q[0]), oracle.to_f64(km[0]), oracle.to_f64(vm[0]), skipped,
                                      oracle.to_f64(ks[0]), oracle.to_f64(vs[0]), 128, 1 / math.sqrt(192))
     assert np.abs(out.cpu().numpy()[0] - ref).max() <= 1e-2
+
+
+# ------------------------------------------------------------------ fused scoring + Top-k
+
+@pytest.mark.parametrize("mode", ["flat", "pooled", "generic"])
+def test_index_topk_fused(csa2, mode):
+    rng = np.random.default_rng(12)
+    B, N, P, K = 5, 4096, 64, 256
+    kw = dict(batch=B, n_entries=N, pool_blocks=P, topk=K)
+    if mode == "generic":
+        kw.update(idx_heads=4, idx_dim=16)
+    sh = _shape(**kw)
+    HI, dI = sh.idx_heads, sh.idx_dim
+    k_idx = _int_keys(rng, (B, N, dI))
+    q_idx = _int_keys(rng, (B, HI, dI))
+    w = rng.integers(1, 4, size=(B, HI)).astype(np.float32)
+    n_valid = np.array([N, N - 5, 8 * P - 3, 100, 0], dtype=np.int32)
+    ws = csa2.workspace(sh)
+    pool = n_pool = None
+    if mode != "flat":
+        kb = torch.zeros((B, N // 8, dI), dtype=torch.bfloat16, device="cuda")
+        csa2.block_keys(sh, bf16(k_idx), i32(n_valid), kb, ws, round_to_int=True)
+        pool = torch.zeros((B, P), dtype=torch.int32, device="cuda")
+        n_pool = torch.zeros(B, dtype=torch.int32, device="cuda")
+        csa2.index_blocks(sh, bf16(q_idx), f32(w), kb, i32(n_valid), pool, n_pool, ws)
+    for k in (K, 37):
+        idx = torch.full((B, k), -9, dtype=torch.int32, device="cuda")
+        n_out = torch.zeros(B, dtype=torch.int32, device="cuda")
+        csa2.index_topk(sh, bf16(q_idx), f32(w), bf16(k_idx), i32(n_valid), k, idx, ws, pool=pool, n_pool=n_pool,
+                        n_out=n_out)
+        got = idx.cpu().numpy()
+        for b in range(B):
+            keys = oracle.to_f64(k_idx[b])
+            n = int(n_valid[b])
+            kb_o = oracle.block_keys(keys, n, 8, True) if mode != "flat" else None
+            r = oracle.layer_indices(oracle.to_f64(q_idx[b]), w[b].astype(np.float64), keys, kb_o, n, topk=k,
+                                     block=8, pool=P, hier=mode != "flat")
+            assert got[b].tolist() == r["idx"].tolist(), f"{mode} k={k} query {b}"
+            assert int(n_out.cpu().numpy()[b]) == int((r["idx"] >= 0).sum())
+    assert_no_device_error(csa2, ws)
