@@ -64,7 +64,7 @@ def algorithmic_bytes(wl) -> dict:
         ns = int(wl.n_swa[b])
         nb = -(-nv // sh.block)
         for L in wl.layers:
-            if L.mode != W.REUSE:
+            if L.mode in (W.FULL, W.REINDEX):
                 if L.hier:
                     pb = min(sh.pool_blocks, nb)
                     total["indexer_blocks"] += nb * sh.idx_dim * e
@@ -276,10 +276,10 @@ def run_reference(args):
         pool.close()
     total = sum(times)
     value = pool.queries * len(times) / total
-    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": 0 if world == 1 else world,
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * total / len(times),
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-            "config": config_of(wl, args),
+            "config": {k: v for k, v in config_of(wl, args).items() if k not in ("l2", "launch")},
             "cpu_baseline": {"value": value, "unit": UNIT, "cores": pool.workers, "kind": "oracle",
                              "sample": f"{pool.queries} of {wl.shape.batch} queries per step"},
             "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
@@ -457,7 +457,7 @@ def dominant_kernel_roofline(csa2, wl, d, stream, flush, args, peak, peak_src):
     """Time the step's dominant kernel alone (CUDA events on its stream, L2 flushed between launches)."""
     import torch
     sh = wl.shape
-    L0 = next(L for L in d["layers"] if L["mode"] != W.REUSE)
+    L0 = next(L for L in d["layers"] if L["mode"] in (W.FULL, W.REINDEX))
     hier = bool(L0.get("hier"))
     dev = d["k_idx"].device
     reps = max(args.steps, 10)
@@ -540,7 +540,7 @@ def end_to_end(csa2, wl, d, graph, stream, flush, args, dev):
     world = dist_env()[1]
     return {"value": wl.shape.batch * world * steps / total, "unit": UNIT, "h2d_bytes_per_step": h2d,
             "d2h_bytes_per_step": d2h, "ms_per_step": 1e3 * total / steps,
-            "resident": "main KV, SWA-free caches (K/V main, indexer keys, block keys) stay on the device"}
+            "resident": "the main-KV, indexer-key and block-key caches stay on the device"}
 
 
 def main(argv=None):

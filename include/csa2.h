@@ -66,7 +66,10 @@ typedef enum {
   CSA2_ERR_TIMEOUT = -6       /* returned by csa2_read_device_error: a bounded device wait gave up */
 } csa2_status;
 
-typedef enum { CSA2_FULL = 0, CSA2_REINDEX = 1, CSA2_REUSE = 2 } csa2_mode;
+/* CSA2_SWA: a pure sliding-window layer (the first two encoder layers of the
+ * architecture figure caption): it attends only its own SWA rows and neither
+ * needs nor produces indices. */
+typedef enum { CSA2_FULL = 0, CSA2_REINDEX = 1, CSA2_REUSE = 2, CSA2_SWA = 3 } csa2_mode;
 typedef enum { CSA2_BF16 = 0, CSA2_F32 = 1 } csa2_dtype;
 
 /* Problem shape shared by a layer group.  Symbols: B batch (one decode query
@@ -95,13 +98,13 @@ typedef struct {
   int32_t mode;        /* csa2_mode */
   int32_t hier;        /* 1: hierarchical (block pool) indexing; needs kb and pool_blocks > 0 */
   const void* q;       /* [B, H, dk] the layer's own query */
-  const void* q_idx;   /* [B, HI, dI] indexer query (Full / Reindex; ignored for Reuse) */
-  const float* w_idx;  /* [B, HI] indexer head weights (Full / Reindex; ignored for Reuse) */
+  const void* q_idx;   /* [B, HI, dI] indexer query (Full / Reindex; ignored for Reuse and SWA) */
+  const float* w_idx;  /* [B, HI] indexer head weights (Full / Reindex; ignored for Reuse and SWA) */
   const void* k_swa;   /* [B, W, dk] the layer's own SWA keys, oldest first */
   const void* v_swa;   /* [B, W, dv] the layer's own SWA values */
   float* out;          /* [B, H, dv] attention output */
   float* lse;          /* [B, H] natural-log sum of exp of the scaled logits, or NULL */
-  int32_t* idx_out;    /* [B, K] fresh indices of an indexing layer, or NULL; untouched for Reuse */
+  int32_t* idx_out;    /* [B, K] fresh indices of an indexing layer, or NULL; untouched for Reuse / SWA */
 } csa2_layer;
 
 /* Workspace bytes needed by any entry point for this shape (host only). */
@@ -190,7 +193,8 @@ int csa2_sparse_attn(const csa2_shape* shape, const void* q, const void* k_main,
 /* A whole layer group over one shared main KV and indexer-key cache (the
  * group's Full layer's): layers run in order; Full and Reindex compute fresh
  * indices (flat, or hierarchical when layer.hier), Reuse attends with the
- * latest indices; every layer attends with its own q and SWA KV.
+ * latest indices; every layer attends with its own q and SWA KV; an SWA
+ * layer attends its SWA rows only.
  * Rules: a Reuse layer needs an earlier Full or Reindex layer in the group;
  * hier needs kb (from csa2_block_keys) and pool_blocks > 0.
  *   k_main [B, N, dk]  v_main [B, N, dv]  k_idx [B, N, dI]

@@ -33,7 +33,9 @@ What it computes, in plain numpy, without blocking, fusion or reordering:
 * layer groups -- Full computes fresh indices, Reindex computes fresh
   indices with its own indexer query over the shared keys, Reuse takes the
   latest indices; every layer has its own query and SWA KV (page 3, "CSA2
-  with cross-layer reuse", mode table and the sentence after it).
+  with cross-layer reuse", mode table and the sentence after it).  A pure
+  sliding-window layer (page 3 figure caption: the first two encoder layers)
+  attends its SWA rows only.
 
 Parity pins: every function above is pinned by ``tests/test_oracle_pins.py``
 (textbook dense attention, closed forms, brute-force selection, a
@@ -49,7 +51,7 @@ from typing import Dict, List, Optional
 
 import numpy as np
 
-FULL, REINDEX, REUSE = 0, 1, 2
+FULL, REINDEX, REUSE, SWA = 0, 1, 2, 3
 
 
 # ----------------------------------------------------------------------------
@@ -225,6 +227,13 @@ def run_group(wl, *, queries: Optional[List[int]] = None, want_attention: bool =
         cur = None
         for li, L in enumerate(wl.layers):
             r = results[li]
+            if L.mode == SWA:
+                if want_attention:
+                    out, lse = attend(to_f64(L.q[b]), to_f64(L.k_swa[b])[:n_swa], to_f64(L.v_swa[b])[:n_swa],
+                                      scale)
+                    r.setdefault("out", np.zeros((len(qs), sh.q_heads, sh.v_dim)))[bi] = out
+                    r.setdefault("lse", np.zeros((len(qs), sh.q_heads)))[bi] = lse
+                continue
             if L.mode == REUSE:
                 if cur is None:
                     raise ValueError("a Reuse layer needs an earlier indexing layer in the group")
@@ -250,11 +259,11 @@ def run_group(wl, *, queries: Optional[List[int]] = None, want_attention: bool =
 def group_counts(modes: List[object]) -> Dict[str, int]:
     """Counts over a layer pattern: CSA2 layers, layers storing global KV, indexer layers.
 
-    ``modes`` holds FULL/REINDEX/REUSE or the string "swa" for a pure
-    sliding-window layer.  Only Full layers compute (store) their own main KV;
+    ``modes`` holds FULL/REINDEX/REUSE, and SWA (or the string "swa") for a
+    pure sliding-window layer.  Only Full layers compute (store) their own main KV;
     Full and Reindex layers run an indexer (page 3, mode table).
     """
-    csa2 = [m for m in modes if m != "swa"]
+    csa2 = [m for m in modes if m not in ("swa", SWA)]
     return {
         "layers": len(modes),
         "csa2": len(csa2),

@@ -17,7 +17,7 @@ import torch
 HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(HERE, "libcsa2.so")
 
-FULL, REINDEX, REUSE = 0, 1, 2
+FULL, REINDEX, REUSE, SWA = 0, 1, 2, 3
 BF16, F32 = 0, 1
 
 OK = 0
@@ -325,7 +325,7 @@ def upload(wl, device="cuda", with_outputs: bool = True):
         if with_outputs:
             y["out"] = torch.empty((sh.batch, sh.q_heads, sh.v_dim), dtype=torch.float32, device=device)
             y["lse"] = torch.empty((sh.batch, sh.q_heads), dtype=torch.float32, device=device)
-            if L.mode != REUSE:
+            if L.mode in (FULL, REINDEX):
                 y["idx_out"] = torch.empty((sh.batch, sh.topk), dtype=torch.int32, device=device)
         layers.append(y)
     d["layers"] = layers

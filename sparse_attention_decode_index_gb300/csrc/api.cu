@@ -218,7 +218,7 @@ int do_topk(const csa2_shape& s, const WsLayout& L, void* ws, const float* score
 
 int do_attn(const csa2_shape& s, const void* q, const void* k_main, const void* v_main, const int32_t* idx,
             const void* k_swa, const void* v_swa, const int32_t* n_swa, float* out, float* lse, int* err,
-            cudaStream_t st) {
+            cudaStream_t st, bool swa_only = false) {
   AttnArgs a{};
   a.q = q;
   a.k_main = k_main;
@@ -230,7 +230,7 @@ int do_attn(const csa2_shape& s, const void* q, const void* k_main, const void* 
   a.out = out;
   a.lse = lse;
   a.n_entries = s.n_entries;
-  a.topk = s.topk;
+  a.topk = swa_only ? 0 : s.topk;   // a pure SWA layer has no main-KV slots
   a.swa = s.swa;
   a.heads = s.q_heads;
   a.k_dim = s.k_dim;
@@ -446,10 +446,15 @@ int csa2_layer_group(const csa2_shape* shape, const csa2_layer* layers, int32_t 
   bool have_idx = false;
   for (int l = 0; l < n_layers; ++l) {
     const csa2_layer& y = layers[l];
-    if (y.mode != CSA2_FULL && y.mode != CSA2_REINDEX && y.mode != CSA2_REUSE) return CSA2_ERR_INVALID_ARG;
+    if (y.mode != CSA2_FULL && y.mode != CSA2_REINDEX && y.mode != CSA2_REUSE && y.mode != CSA2_SWA)
+      return CSA2_ERR_INVALID_ARG;
     if (y.hier != 0 && y.hier != 1) return CSA2_ERR_INVALID_ARG;
     CSA2_TRY(check_attn_args(s, y.q, k_main, v_main, y.out));
     CSA2_TRY(check_sswa(s, y.k_swa, y.v_swa, n_swa));
+    if (y.mode == CSA2_SWA) {
+      if (s.swa < 1) return CSA2_ERR_INVALID_ARG;
+      continue;
+    }
     if (y.mode == CSA2_REUSE) {
       if (!have_idx) return CSA2_ERR_INVALID_ARG;
       continue;
@@ -466,6 +471,10 @@ int csa2_layer_group(const csa2_shape* shape, const csa2_layer* layers, int32_t 
   const int32_t* cur = nullptr;
   for (int l = 0; l < n_layers; ++l) {
     const csa2_layer& y = layers[l];
+    if (y.mode == CSA2_SWA) {
+      CSA2_TRY(do_attn(s, y.q, k_main, v_main, nullptr, y.k_swa, y.v_swa, n_swa, y.out, y.lse, err, stream, true));
+      continue;
+    }
     if (y.mode != CSA2_REUSE) {
       int32_t* dst = y.idx_out != nullptr ? y.idx_out : at<int32_t>(ws, L.idx);
       float* ts = at<float>(ws, L.tok_scores);

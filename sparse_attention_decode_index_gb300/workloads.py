@@ -28,6 +28,9 @@ plus a 128-token SWA window, blocks of 8, a pool of at most 2,048 blocks):
   2,048 blocks.
 * ``dec_b16_1m`` -- decoder group Full + 3 Reuse + [Reindex + 3 Reuse] x 4,
   batch 16, 1,048,576 tokens at ratio 4 (262,144 entries).
+* ``enc_stack_b32_32k`` -- the whole 20-layer encoder stack SWA, SWA,
+  [Full + 5 Reuse] x 3 at the shapes of ``enc_b32_32k`` (pure SWA layers attend
+  their window only).
 
 Value recipe: main and SWA keys N(0,1)/sqrt(k_dim), values
 N(0,1)/sqrt(v_dim), queries N(0,1), all rounded to bf16; indexer queries
@@ -43,8 +46,8 @@ from typing import List, Optional
 
 import numpy as np
 
-FULL, REINDEX, REUSE = 0, 1, 2
-MODE_NAMES = {FULL: "full", REINDEX: "reindex", REUSE: "reuse"}
+FULL, REINDEX, REUSE, SWA = 0, 1, 2, 3
+MODE_NAMES = {FULL: "full", REINDEX: "reindex", REUSE: "reuse", SWA: "swa"}
 
 
 def f32_to_bf16_bits(x: np.ndarray) -> np.ndarray:
@@ -160,6 +163,11 @@ def encoder_group_modes(n_reuse: int = 5) -> List[int]:
     return [FULL] + [REUSE] * n_reuse
 
 
+def encoder_stack_modes() -> List[int]:
+    """Encoder stack of the architecture figure: SWA, SWA, then [Full + 5 Reuse] x 3 (20 layers)."""
+    return [SWA, SWA] + encoder_group_modes(5) * 3
+
+
 def decoder_group_modes() -> List[int]:
     """Decoder stack: Full + 3 Reuse, then [Reindex + 3 Reuse] x 4 (20 layers)."""
     return [FULL] + [REUSE] * 3 + ([REINDEX] + [REUSE] * 3) * 4
@@ -202,7 +210,7 @@ def make_workload(shape: Shape, modes: List[int], *, seed: int = 0, cfg_id: int 
         k_swa = kv((seed, cfg_id, 11, l), (B, shape.swa, shape.k_dim), shape.k_dim)
         v_swa = kv((seed, cfg_id, 12, l), (B, shape.swa, shape.v_dim), shape.v_dim)
         q_idx = w = None
-        if mode != REUSE:
+        if mode in (FULL, REINDEX):
             q_idx = idxv((seed, cfg_id, 13, l), (B, shape.idx_heads, shape.idx_dim))
             if f32:
                 w = np.ones((B, shape.idx_heads), dtype=np.float32)
@@ -254,6 +262,8 @@ WORKLOADS = {
                         pool=0, context=32768),
     "reindex_b64_128k": dict(cfg_id=3, batch=64, n_entries=32768, modes=[REINDEX], pool=2048,
                              context=131072),
+    "enc_stack_b32_32k": dict(cfg_id=5, batch=32, n_entries=8192, modes=encoder_stack_modes(), pool=0,
+                              context=32768),
     "dec_b16_1m": dict(cfg_id=4, batch=16, n_entries=262144, modes=decoder_group_modes(),
                        pool=2048, context=1048576),
 }

@@ -4,7 +4,7 @@ import numpy as np
 import pytest
 
 import oracle
-from oracle import FULL, REINDEX, REUSE
+from oracle import FULL, REINDEX, REUSE, SWA
 from sparse_attention_decode_index_gb300 import workloads as W
 from tests.gpu_helpers import assert_no_device_error, compare_attention, lib_ready, need_gpu, torch
 
@@ -35,7 +35,9 @@ def check_group(csa2, wl, d, queries=None, atol=1e-2):
     cur = None
     for li, L in enumerate(wl.layers):
         y, r = d["layers"][li], ref[li]
-        if L.mode != REUSE:
+        if L.mode == SWA:
+            pass
+        elif L.mode != REUSE:
             got = y["idx_out"].cpu().numpy()[qs]
             assert np.array_equal(got, r["idx"]), f"layer {li} ({W.MODE_NAMES[L.mode]}): indices differ"
             cur = y["idx_out"]
@@ -54,6 +56,7 @@ def check_group(csa2, wl, d, queries=None, atol=1e-2):
     ("enc_b32_32k", None),
     ("reindex_b64_128k", [0, 1, 31, 63]),
     ("dec_b16_1m", [0, 9]),
+    ("enc_stack_b32_32k", [0, 5, 31]),
 ])
 def test_named_workload(csa2, name, queries):
     wl = W.named(name)
@@ -180,5 +183,13 @@ def test_all_equal_scores_pick_lowest_indices(csa2):
 def test_small_topk_and_window_batch_one(csa2):
     wl = _small_group([FULL, REUSE, REINDEX], batch=1, n_entries=4096, topk=64, swa=16, pool=8,
                       n_valid=[3001])
+    d = run_gpu(csa2, wl)
+    check_group(csa2, wl, d)
+
+
+def test_swa_layers_anywhere_in_a_group(csa2):
+    """Pure sliding-window layers need no indices: first, between and after CSA2 layers."""
+    wl = _small_group([SWA, FULL, SWA, REUSE, REINDEX, SWA], n_valid=[2048, 1500, 9, 0, 2048, 700],
+                      n_swa=[128, 0, 5, 128, 1, 64], pool=32)
     d = run_gpu(csa2, wl)
     check_group(csa2, wl, d)

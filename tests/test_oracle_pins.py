@@ -189,7 +189,7 @@ def test_reuse_layers_return_the_indexing_layers_indices():
 
 
 def test_group_counts_of_the_40_layer_pattern():
-    enc = ["swa", "swa"] + W.encoder_group_modes(5) * 3
+    enc = W.encoder_stack_modes()
     dec = W.decoder_group_modes()
     assert len(enc) == 20 and len(dec) == 20
     c = oracle.group_counts(enc + dec)
@@ -288,3 +288,20 @@ def test_attention_closed_forms():
     # the softmax scale multiplies the logits (a doubled scale != the original)
     c, _ = oracle.sparse_attention(q, k_main, v_main, idx, k_swa, v_swa, 4, 0.8)
     assert not np.allclose(a, c)
+
+
+def test_swa_layer_is_window_only_attention():
+    """A pure sliding-window layer equals textbook attention over its window rows."""
+    sh = W.Shape(batch=2, n_entries=64, idx_heads=2, idx_dim=8, block=8, pool_blocks=0, topk=6, q_heads=2,
+                 k_dim=5, v_dim=3, swa=7)
+    wl = W.make_workload(sh, [W.SWA, W.FULL, W.SWA], seed=9, n_swa=[7, 3])
+    res = oracle.run_group(wl)
+    for li in (0, 2):
+        L = wl.layers[li]
+        for b in range(2):
+            ns = int(wl.n_swa[b])
+            ref_out, ref_lse = _naive_dense(oracle.to_f64(L.q[b]).tolist(), oracle.to_f64(L.k_swa[b])[:ns].tolist(),
+                                            oracle.to_f64(L.v_swa[b])[:ns].tolist(), 1 / math.sqrt(5))
+            assert np.allclose(res[li]["out"][b], ref_out, atol=1e-12)
+            assert np.allclose(res[li]["lse"][b], ref_lse, atol=1e-12)
+    assert "idx" not in res[0]
