@@ -162,6 +162,10 @@ CSA2_DEV void cluster_sync_all() {
   asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
 }
 
+// Split form of cluster_sync_all: local work may run between the two halves.
+CSA2_DEV void cluster_arrive() { asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory"); }
+CSA2_DEV void cluster_wait() { asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory"); }
+
 // Address of the same shared variable in CTA `rank` of this cluster.
 CSA2_DEV uint32_t dsmem_addr(const void* p, uint32_t rank) {
   uint32_t r;
@@ -175,6 +179,16 @@ CSA2_DEV void dsmem_st_f32(uint32_t addr, float v) {
 
 CSA2_DEV void dsmem_st_v2(uint32_t addr, float x, float y) {
   asm volatile("st.shared::cluster.v2.f32 [%0], {%1, %2};" ::"r"(addr), "f"(x), "f"(y) : "memory");
+}
+
+CSA2_DEV void dsmem_st_v2u(uint32_t addr, uint32_t x, uint32_t y) {
+  asm volatile("st.shared::cluster.v2.u32 [%0], {%1, %2};" ::"r"(addr), "r"(x), "r"(y) : "memory");
+}
+
+CSA2_DEV void dsmem_st_v4u(uint32_t addr, uint4 v) {
+  asm volatile("st.shared::cluster.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(v.x), "r"(v.y), "r"(v.z),
+               "r"(v.w)
+               : "memory");
 }
 
 CSA2_DEV float dsmem_ld_f32(uint32_t addr) {

@@ -8,15 +8,30 @@
 // streaming indexer kernel (one producer warp feeding a TMA bulk-copy ring,
 // four consumer warps running mma.sync m16n8k16 on q_idx . K^T).  Instead of
 // writing the scores to global memory, each CTA keeps their order keys in
-// shared memory.  The cluster then selects the Top-k under (score descending,
-// index ascending) with a distributed radix select: every pass builds a local
-// 256-bin histogram (in the now idle ring buffer),
-// publishes its totals, and after one cluster barrier every CTA sums the C
-// totals through distributed shared memory and keeps the same bin.  Each bin
-// has 8 counter copies (one per lane & 7), which keeps the clear and the
-// reduction cheap while bounding same-address contention to 4 lanes.  The tie
-// quota and output offset of each CTA come from a prefix over the CTAs, and
-// because the CTAs hold ascending index ranges the selected ids are written
+// shared memory and the cluster selects the Top-k under (score descending,
+// index ascending) with three cluster barriers in the common case:
+//
+//   1. every CTA pushes (count, min, max) of its keys into every CTA;
+//   2. a radix pass: every CTA histograms its keys into 256 bins over the
+//      common [min, max] range and pushes the bin totals into every CTA, so
+//      that after the barrier each CTA holds all C histograms and finds the
+//      bin holding the k-th key, the keys above it, and each CTA's share of
+//      both;
+//   3. every CTA pushes its keys inside that bin into every CTA, which then
+//      finishes the selection alone (passes over the gathered keys, each
+//      narrowing to the exact [min, max] of the chosen bin) and counts each
+//      CTA's keys above and at the threshold.
+//
+// Only while the chosen bin holds more keys than a CTA can gather do steps 1
+// and 2 repeat on the keys of that bin.  The first pass of each loop bins the
+// score values linearly between the range's end points (a monotone map, so
+// every bin is a contiguous key range); later passes bin the order-key bits,
+// which removes at least 8 bits of the range per pass.
+//
+// All remote traffic is stores into the destination's shared memory, so no
+// step waits on a remote load.  Ties at the threshold go to the lowest
+// indices: the CTAs hold ascending index ranges, so each CTA's quota and
+// output offset follow from the per-CTA counts, and each CTA writes its ids
 // directly in ascending order.
 //
 // (DeepSeek V4.1 Flash architecture page: bullet "Hierarchical indexer" -- block
@@ -41,22 +56,76 @@ constexpr int kBlock = 8;
 constexpr int kBlockBytes = kBlock * kRowBytes;
 constexpr int kBlocksPerTile = kTileRows / kBlock;
 constexpr int kBins = 256;
-constexpr int kCopies = 8;                           // counter copies per bin (lane & 7)
 constexpr int kMaxCluster = 8;
 constexpr int kMaxRowsPerCta = 4096;                 // order keys kept in shared memory
+// After scoring, the ring buffer is reused:
+//   region A: the histogram of a cluster-wide pass, two bins per word (16-bit
+//             counters, 32 lane-private copies), then the gather buffer;
+//   region B: the pushed per-CTA bin totals (two buffers), then the
+//             histogram (8 copies) and totals of the passes over gathered keys.
+constexpr int kRingWords = kStages * kTileBytes / 4;
+constexpr int kLanes = 32;
+constexpr int kHistDWords = (kBins / 2) * kLanes;
+constexpr int kGatherCap = kRingWords - 2 * kMaxCluster * kBins;   // words of region A
+constexpr int kTotWords = kMaxCluster * kBins;                      // one totals buffer
+constexpr int kCopiesL = 8;
 
-static_assert(kBins * kCopies * 4 <= kStages * kTileBytes, "histogram reuses the ring buffer");
+static_assert(kHistDWords <= kGatherCap, "histogram fits region A");
+static_assert(kBins * kCopiesL + kBins <= 2 * kTotWords, "local histogram fits region B");
+static_assert(kMaxRowsPerCta < 65536, "16-bit histogram counters");
 
 struct SelSmall {
-  uint32_t tot[2][kBins];
-  uint32_t gtot[kBins];
+  uint4 stats[kMaxCluster];        // pushed by every CTA: (keys, min key, max key, 0)
   uint32_t red[3][kWarpsAll];
-  uint32_t stats[3];    // this CTA: valid count, min key, max key
-  uint32_t fin[2];      // this CTA: count > T, count == T
-  uint32_t sel_bin, sel_above, lo, hi, n_valid, offset, quota;
+  uint32_t above_r[kMaxCluster];   // per CTA: keys above the current range
+  uint32_t cnt_r[kMaxCluster];     // per CTA: keys inside the current range
+  uint32_t gt_r[kMaxCluster];      // per CTA: keys above the threshold
+  uint32_t eq_r[kMaxCluster];      // per CTA: keys at the threshold
+  uint32_t sel_bin, sel_above, gcount;
   uint64_t full[kStages];
   uint64_t empty[kStages];
 };
+
+// A monotone map of the order keys inside [lo, hi] to kBins bins: either
+// linear in the score value (first passes) or the top bits of (key - lo).
+struct Binning {
+  uint32_t lo;
+  int shift;
+  float vlo, scale;
+  bool lin;
+};
+
+__device__ __forceinline__ Binning make_binning(uint32_t lo, uint32_t hi, bool allow_linear) {
+  Binning bn;
+  bn.lo = lo;
+  const int bits = 32 - __clz(hi - lo);
+  bn.shift = bits > 8 ? bits - 8 : 0;
+  bn.lin = false;
+  bn.vlo = 0.f;
+  bn.scale = 0.f;
+  if (allow_linear) {
+    const float x = key_score(lo), y = key_score(hi);
+    const float d = __fsub_rn(y, x);
+    if (isfinite(x) && isfinite(y) && isfinite(d) && d > 0.f) {
+      const float sc = __fdiv_rn(float(kBins), d);
+      if (isfinite(sc) && sc > 0.f) {
+        bn.lin = true;
+        bn.vlo = x;
+        bn.scale = sc;
+      }
+    }
+  }
+  return bn;
+}
+
+// Bin of a key inside [lo, hi]: non-decreasing in the key, 0 at lo.
+__device__ __forceinline__ uint32_t bin_of(uint32_t key, const Binning& bn) {
+  if (bn.lin) {
+    const float x = __fmul_rn(__fsub_rn(key_score(key), bn.vlo), bn.scale);
+    return min(uint32_t(kBins - 1), __float2uint_rz(x));
+  }
+  return (key - bn.lo) >> bn.shift;
+}
 
 constexpr size_t kOffSmall = size_t(kStages) * kTileBytes;
 constexpr size_t kOffKeys = kOffSmall + ((sizeof(SelSmall) + 127) / 128) * 128;
@@ -67,19 +136,17 @@ size_t select_smem_bytes(int rows_per_cta, bool pooled) {
 }
 
 template <bool POOLED>
-__global__ void __launch_bounds__(kThreads) index_select_kernel(const SelectArgs a) {
+__global__ void __launch_bounds__(kThreads, 4) index_select_kernel(const SelectArgs a) {
   extern __shared__ __align__(1024) uint8_t smem[];
   uint8_t* tiles = smem;
   SelSmall& sm = *reinterpret_cast<SelSmall*>(smem + kOffSmall);
   uint32_t* s_key = reinterpret_cast<uint32_t*>(smem + kOffKeys);
   const int units_cap = a.rows_per_cta;                                 // rows (flat) or blocks (pooled)
   int* s_pool = reinterpret_cast<int*>(s_key + (POOLED ? units_cap * kBlock : units_cap));
-  uint32_t(*hist)[kCopies] = reinterpret_cast<uint32_t(*)[kCopies]>(smem);   // after scoring
 
   const int b = blockIdx.y;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const uint32_t crank = cluster_rank(), ncta = cluster_size();
-  pdl_launch_dependents();
 
   const int nv = clamp_count(a.n_valid[b], a.valid_cap, a.err);
   if (tid == 0) {
@@ -220,109 +287,301 @@ __global__ void __launch_bounds__(kThreads) index_select_kernel(const SelectArgs
   __syncthreads();   // all keys written; the ring buffer is free for the histogram
 
   // ---------------- phase 2: cluster-wide exact Top-k over the keys
-  // (count, min, max) of the keys, tracked while scoring
-  {
-    uint32_t cnt = my_cnt, lo = my_lo, hi = my_hi;
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) {
-      cnt += __shfl_xor_sync(0xffffffffu, cnt, o);
-      lo = min(lo, __shfl_xor_sync(0xffffffffu, lo, o));
-      hi = max(hi, __shfl_xor_sync(0xffffffffu, hi, o));
+  uint32_t* ring = reinterpret_cast<uint32_t*>(smem);
+  uint32_t* histD = ring;                                 // [kBins / 2][kLanes], 16-bit pairs
+  uint32_t* gk = ring;                                    // gathered keys, per-CTA segments
+  uint32_t* tot = ring + kGatherCap;                      // [2][kMaxCluster][kBins]
+  uint32_t* histL = tot;                                  // [kBins][kCopiesL]
+  uint32_t* totL = tot + kBins * kCopiesL;                // [kBins]
+  const uint32_t k = uint32_t(a.k);
+  if (tid == 0) sm.gcount = 0u;
+  if (tid < kMaxCluster) sm.above_r[tid] = 0u;
+
+  // Selected: every key > T, plus the first q keys == T in index order.
+  uint32_t T = 0u, q = 0u;
+  uint32_t lo = 0u, hi = 0xffffffffu, need = k;
+  Binning flt{};                 // the members are the keys in [lo, hi] inside bin fsel of flt
+  uint32_t fsel = 0u;
+  bool filtered = false, gathered = false, resolved = false;
+  uint32_t n_all = 0u;           // valid candidates of the query
+  for (int step = 0; step < 12 && !resolved; ++step) {
+    // (1) count, min and max of the members in every CTA, pushed to every CTA
+    {
+      uint32_t c = my_cnt, l = my_lo, h = my_hi;   // step 0: tracked while scoring
+      if (step > 0) {
+        c = 0u;
+        l = 0xffffffffu;
+        h = 0u;
+        for (int j = tid; j < rows_total; j += kThreads) {
+          const uint32_t kk = s_key[j];
+          if (kk != 0u && kk >= lo && kk <= hi && (!filtered || bin_of(kk, flt) == fsel)) {
+            ++c;
+            l = min(l, kk);
+            h = max(h, kk);
+          }
+        }
+      }
+      c = __reduce_add_sync(0xffffffffu, c);
+      l = __reduce_min_sync(0xffffffffu, l);
+      h = __reduce_max_sync(0xffffffffu, h);
+      if (lane == 0) {
+        sm.red[0][warp] = c;
+        sm.red[1][warp] = l;
+        sm.red[2][warp] = h;
+      }
+      __syncthreads();
+      if (tid < int(ncta)) {
+        uint4 v = make_uint4(0u, 0xffffffffu, 0u, 0u);
+        for (int w = 0; w < kWarpsAll; ++w) {
+          v.x += sm.red[0][w];
+          v.y = min(v.y, sm.red[1][w]);
+          v.z = max(v.z, sm.red[2][w]);
+        }
+        dsmem_st_v4u(dsmem_addr(&sm.stats[crank], uint32_t(tid)), v);
+      }
+      cluster_arrive();
+      uint4* hv = reinterpret_cast<uint4*>(histD);   // region A is written by no other CTA here
+      for (int j = tid; j < kHistDWords / 4; j += kThreads) hv[j] = make_uint4(0u, 0u, 0u, 0u);
+      __syncthreads();
+      cluster_wait();
     }
-    if (lane == 0) {
-      sm.red[0][warp] = cnt;
-      sm.red[1][warp] = lo;
-      sm.red[2][warp] = hi;
+    uint32_t n = 0u, glo = 0xffffffffu, ghi = 0u;
+    for (int r = 0; r < int(ncta); ++r) {
+      const uint4 v = sm.stats[r];
+      n += v.x;
+      if (v.x != 0u) {
+        glo = min(glo, v.y);
+        ghi = max(ghi, v.z);
+      }
+    }
+    if (step == 0) n_all = n;
+    if (step == 0 && n <= k) {   // every candidate is selected
+      if (tid < int(ncta)) {
+        sm.gt_r[tid] = sm.stats[tid].x;
+        sm.eq_r[tid] = 0u;
+      }
+      resolved = true;
+      break;
+    }
+    lo = glo;   // the members are exactly the keys in [lo, hi] (bins are contiguous key ranges)
+    hi = ghi;
+    if (n == need) {
+      T = lo - 1u;
+      q = 0u;
+      if (tid < int(ncta)) {
+        sm.gt_r[tid] = sm.above_r[tid] + sm.stats[tid].x;
+        sm.eq_r[tid] = 0u;
+      }
+      resolved = true;
+      break;
+    }
+    if (lo == hi) {
+      T = lo;
+      q = need;
+      if (tid < int(ncta)) {
+        sm.gt_r[tid] = sm.above_r[tid];
+        sm.eq_r[tid] = sm.stats[tid].x;
+      }
+      resolved = true;
+      break;
+    }
+
+    // (2) radix pass over [lo, hi]: every CTA's bin totals pushed to every CTA
+    const Binning bn = make_binning(lo, hi, step == 0);
+    for (int j0 = tid; j0 < rows_total; j0 += 8 * kThreads) {
+      uint32_t kk[8];
+#pragma unroll
+      for (int u = 0; u < 8; ++u) kk[u] = j0 + u * kThreads < rows_total ? s_key[j0 + u * kThreads] : 0u;
+#pragma unroll
+      for (int u = 0; u < 8; ++u)
+        if (kk[u] != 0u && kk[u] >= lo && kk[u] <= hi) {
+          const uint32_t bin = bin_of(kk[u], bn);
+          atomicAdd(&histD[(bin >> 1) * kLanes + lane], (bin & 1u) ? 0x10000u : 1u);
+        }
     }
     __syncthreads();
-    if (tid == 0) {
-      uint32_t c = 0, l = 0xffffffffu, h = 0u;
-      for (int w = 0; w < kWarpsAll; ++w) {
-        c += sm.red[0][w];
-        l = min(l, sm.red[1][w]);
-        h = max(h, sm.red[2][w]);
-      }
-      sm.stats[0] = c;
-      sm.stats[1] = l;
-      sm.stats[2] = h;
+    const int buf = step & 1;
+    if (tid < kBins / 2) {   // rotated reads: conflict-free
+      const uint32_t* row = histD + tid * kLanes;
+      uint32_t sum = 0u;
+#pragma unroll 8
+      for (int c = 0; c < kLanes; ++c) sum += row[(c + tid) & (kLanes - 1)];
+      uint32_t* dst = tot + buf * kTotWords + crank * kBins + 2 * tid;
+      for (int r = 0; r < int(ncta); ++r) dsmem_st_v2u(dsmem_addr(dst, uint32_t(r)), sum & 0xffffu, sum >> 16);
     }
     cluster_sync_all();
-    if (tid == 0) {
-      uint32_t rc[kMaxCluster], rl[kMaxCluster], rh[kMaxCluster];
+    if (warp == 0) {
+      // lane l holds bins 255 - 8l - j (j = 0..7); first their totals over the CTAs
+      const uint32_t* tb = tot + buf * kTotWords;
+      const int b0 = kBins - 8 - 8 * lane;
+      uint32_t g[8] = {0u, 0u, 0u, 0u, 0u, 0u, 0u, 0u};
+      for (int r = 0; r < int(ncta); ++r) {
+        const uint4 x = *reinterpret_cast<const uint4*>(tb + r * kBins + b0);
+        const uint4 y = *reinterpret_cast<const uint4*>(tb + r * kBins + b0 + 4);
+        g[0] += y.w; g[1] += y.z; g[2] += y.y; g[3] += y.x;
+        g[4] += x.w; g[5] += x.z; g[6] += x.y; g[7] += x.x;
+      }
+      uint32_t local = 0u;
 #pragma unroll
-      for (int r = 0; r < kMaxCluster; ++r) {
-        if (r < int(ncta)) {
-          rc[r] = __float_as_uint(dsmem_ld_f32(dsmem_addr(&sm.stats[0], r)));
-          rl[r] = __float_as_uint(dsmem_ld_f32(dsmem_addr(&sm.stats[1], r)));
-          rh[r] = __float_as_uint(dsmem_ld_f32(dsmem_addr(&sm.stats[2], r)));
-        } else {
-          rc[r] = 0u;
-          rl[r] = 0xffffffffu;
-          rh[r] = 0u;
+      for (int j = 0; j < 8; ++j) local += g[j];
+      uint32_t incl = local;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const uint32_t y = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += y;
+      }
+      uint32_t before = incl - local;
+      int fj = -1;
+      uint32_t fabove = 0u;
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        if (fj < 0 && before < need && before + g[j] >= need) {
+          fj = j;
+          fabove = before;
+        }
+        before += g[j];
+      }
+      const unsigned fm = __ballot_sync(0xffffffffu, fj >= 0);
+      const int fl = fm ? __ffs(fm) - 1 : 0;
+      const int sj = max(0, __shfl_sync(0xffffffffu, fj, fl));
+      const uint32_t sabove = __shfl_sync(0xffffffffu, fabove, fl);
+      const uint32_t sel = uint32_t(kBins - 1 - 8 * fl - sj);
+      // then each CTA's keys above the chosen bin and inside it
+      for (int r = 0; r < int(ncta); ++r) {
+        const uint4 x = *reinterpret_cast<const uint4*>(tb + r * kBins + b0);
+        const uint4 y = *reinterpret_cast<const uint4*>(tb + r * kBins + b0 + 4);
+        const uint32_t v[8] = {x.x, x.y, x.z, x.w, y.x, y.y, y.z, y.w};   // bins b0 .. b0 + 7
+        uint32_t ab = 0u, in = 0u;
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+          const uint32_t bin = uint32_t(b0 + j);
+          if (bin > sel) ab += v[j];
+          if (bin == sel) in += v[j];
+        }
+        ab = __reduce_add_sync(0xffffffffu, ab);
+        in = __reduce_add_sync(0xffffffffu, in);
+        if (lane == 0) {
+          sm.above_r[r] += ab;
+          sm.cnt_r[r] = in;
         }
       }
-      uint32_t c = 0, l = 0xffffffffu, h = 0u;
-#pragma unroll
-      for (int r = 0; r < kMaxCluster; ++r) {
-        c += rc[r];
-        if (rc[r] > 0) {
-          l = min(l, rl[r]);
-          h = max(h, rh[r]);
-        }
+      if (lane == 0) {
+        sm.sel_bin = sel;
+        sm.sel_above = sabove;
+        if (fm == 0u) report(a.err, kErrBadCount, -2);   // cannot happen: [lo, hi] holds >= need keys
       }
-      sm.n_valid = c;
-      sm.lo = l;
-      sm.hi = h;
     }
     __syncthreads();
+    need -= sm.sel_above;
+    flt = bn;
+    fsel = sm.sel_bin;
+    filtered = true;
+    uint32_t padded = 0u;
+    for (int r = 0; r < int(ncta); ++r) padded += (sm.cnt_r[r] + 3u) & ~3u;
+    if (padded <= uint32_t(kGatherCap)) {
+      gathered = true;
+      resolved = true;
+    }
   }
-  const uint32_t n_sel_valid = sm.n_valid;
-  const uint32_t k = uint32_t(a.k);
-  const bool take_all = n_sel_valid <= k;
-  uint32_t T = 0u, need_eq = 0u;
-  if (!take_all) {
-    uint32_t lo = sm.lo, hi = sm.hi, above = 0u;
-    int buf = 0;
-    while (lo != hi) {
-      const uint32_t range = hi - lo;
-      const int bits = 32 - __clz(range);
-      const int shift = bits > 8 ? bits - 8 : 0;
-      uint4* hv = reinterpret_cast<uint4*>(&hist[0][0]);
-      for (int j = tid; j < kBins * kCopies / 4; j += kThreads) hv[j] = make_uint4(0u, 0u, 0u, 0u);
+  if (!resolved) report(a.err, kErrBadCount, -3);   // cannot happen: every step narrows the range
+
+  if (gathered) {
+    // (3) every CTA's keys inside the chosen bin, pushed into its segment of every CTA's gather buffer
+    uint32_t my_off = 0u, G = 0u;
+    for (int r = 0; r < int(ncta); ++r) {
+      if (r == int(crank)) my_off = G;
+      G += (sm.cnt_r[r] + 3u) & ~3u;
+    }
+    const uint32_t my_in = sm.cnt_r[crank];
+    for (int j0 = warp * 32; j0 < rows_total; j0 += kThreads) {
+      const int j = j0 + lane;
+      const uint32_t kk = j < rows_total ? s_key[j] : 0u;
+      const bool in = kk != 0u && kk >= lo && kk <= hi && bin_of(kk, flt) == fsel;
+      const unsigned m = __ballot_sync(0xffffffffu, in);
+      if (m != 0u) {
+        uint32_t base = 0u;
+        if (lane == 0) base = atomicAdd(&sm.gcount, uint32_t(__popc(m)));
+        base = __shfl_sync(0xffffffffu, base, 0);
+        if (in) gk[my_off + base + uint32_t(__popc(m & ((1u << lane) - 1u)))] = kk;
+      }
+    }
+    if (tid < 3 && my_in + uint32_t(tid) < ((my_in + 3u) & ~3u)) gk[my_off + my_in + tid] = 0u;
+    __syncthreads();
+    {
+      const int nvec = int((my_in + 3u) >> 2);
+      for (int i = tid; i < nvec; i += kThreads) {
+        const uint32_t* src = gk + my_off + 4 * i;
+        const uint4 v = *reinterpret_cast<const uint4*>(src);
+        for (int r = 0; r < int(ncta); ++r)
+          if (r != int(crank)) dsmem_st_v4u(dsmem_addr(src, uint32_t(r)), v);
+      }
+    }
+    cluster_sync_all();   // the last remote access of the kernel
+
+    // every CTA finishes the selection alone over the G gathered words (0 = padding)
+    uint4* hl = reinterpret_cast<uint4*>(histL);
+    bool done = false;
+    for (int it = 0; it < 12; ++it) {
+      uint32_t mn = 0xffffffffu, mx = 0u, c = 0u;
+      for (int i = tid; i < int(G); i += kThreads) {
+        const uint32_t kk = gk[i];
+        if (kk != 0u && kk >= lo && kk <= hi && bin_of(kk, flt) == fsel) {
+          mn = min(mn, kk);
+          mx = max(mx, kk);
+          ++c;
+        }
+      }
+      for (int j = tid; j < kBins * kCopiesL / 4; j += kThreads) hl[j] = make_uint4(0u, 0u, 0u, 0u);
+      mn = __reduce_min_sync(0xffffffffu, mn);
+      mx = __reduce_max_sync(0xffffffffu, mx);
+      c = __reduce_add_sync(0xffffffffu, c);
+      if (lane == 0) {
+        sm.red[0][warp] = c;
+        sm.red[1][warp] = mn;
+        sm.red[2][warp] = mx;
+      }
       __syncthreads();
-      for (int j0 = tid; j0 < rows_total; j0 += 8 * kThreads) {
-        uint32_t kk[8];
-#pragma unroll
-        for (int u = 0; u < 8; ++u) kk[u] = j0 + u * kThreads < rows_total ? s_key[j0 + u * kThreads] : 0u;
-#pragma unroll
-        for (int u = 0; u < 8; ++u)
-          if (kk[u] != 0u && kk[u] >= lo && kk[u] <= hi)
-            atomicAdd(&hist[(kk[u] - lo) >> shift][lane & (kCopies - 1)], 1u);
+      c = 0u;
+      mn = 0xffffffffu;
+      mx = 0u;
+      for (int w = 0; w < kWarpsAll; ++w) {
+        c += sm.red[0][w];
+        mn = min(mn, sm.red[1][w]);
+        mx = max(mx, sm.red[2][w]);
+      }
+      lo = mn;   // the members are now exactly the keys in [lo, hi]
+      hi = mx;
+      if (c == need) {
+        T = lo - 1u;
+        q = 0u;
+        done = true;
+        break;
+      }
+      if (lo == hi) {
+        T = lo;
+        q = need;
+        done = true;
+        break;
+      }
+      const Binning bl = make_binning(lo, hi, it < 2);
+      for (int i = tid; i < int(G); i += kThreads) {
+        const uint32_t kk = gk[i];
+        if (kk != 0u && kk >= lo && kk <= hi)
+          atomicAdd(&histL[bin_of(kk, bl) * kCopiesL + (lane & (kCopiesL - 1))], 1u);
       }
       __syncthreads();
       for (int bin = tid; bin < kBins; bin += kThreads) {
-        const uint4 x = *reinterpret_cast<const uint4*>(&hist[bin][0]);
-        const uint4 y = *reinterpret_cast<const uint4*>(&hist[bin][4]);
-        sm.tot[buf][bin] = x.x + x.y + x.z + x.w + y.x + y.y + y.z + y.w;
-      }
-      cluster_sync_all();
-      for (int bin = tid; bin < kBins; bin += kThreads) {
-        uint32_t rv[kMaxCluster];
-#pragma unroll
-        for (int r = 0; r < kMaxCluster; ++r)
-          rv[r] = r < int(ncta) ? __float_as_uint(dsmem_ld_f32(dsmem_addr(&sm.tot[buf][bin], r))) : 0u;
-        uint32_t v = 0u;
-#pragma unroll
-        for (int r = 0; r < kMaxCluster; ++r) v += rv[r];
-        sm.gtot[bin] = v;
+        const uint4 x = *reinterpret_cast<const uint4*>(&histL[bin * kCopiesL]);
+        const uint4 y = *reinterpret_cast<const uint4*>(&histL[bin * kCopiesL + 4]);
+        totL[bin] = x.x + x.y + x.z + x.w + y.x + y.y + y.z + y.w;
       }
       __syncthreads();
       if (warp == 0) {
-        uint32_t cnt[8], local = 0u;
+        uint32_t g[8], local = 0u;
 #pragma unroll
         for (int j = 0; j < 8; ++j) {
-          cnt[j] = sm.gtot[kBins - 1 - lane * 8 - j];
-          local += cnt[j];
+          g[j] = totL[kBins - 1 - lane * 8 - j];
+          local += g[j];
         }
         uint32_t incl = local;
 #pragma unroll
@@ -330,141 +589,108 @@ __global__ void __launch_bounds__(kThreads) index_select_kernel(const SelectArgs
           const uint32_t y = __shfl_up_sync(0xffffffffu, incl, o);
           if (lane >= o) incl += y;
         }
-        uint32_t before = above + incl - local;
+        uint32_t before = incl - local;
 #pragma unroll
         for (int j = 0; j < 8; ++j) {
-          if (before < k && before + cnt[j] >= k) {
+          if (before < need && before + g[j] >= need) {
             sm.sel_bin = uint32_t(kBins - 1 - lane * 8 - j);
             sm.sel_above = before;
           }
-          before += cnt[j];
+          before += g[j];
         }
       }
       __syncthreads();
-      const uint32_t bin = sm.sel_bin;
-      above = sm.sel_above;
-      const uint32_t nlo = lo + (bin << shift);
-      const uint32_t width = (1u << shift) - 1u;
-      hi = (hi - nlo > width) ? nlo + width : hi;
-      lo = nlo;
-      buf ^= 1;
+      need -= sm.sel_above;
+      flt = bl;
+      fsel = sm.sel_bin;
     }
-    T = lo;
-    need_eq = k - above;
+    if (!done) report(a.err, kErrBadCount, -3);   // cannot happen: every pass narrows the range
+    // per CTA: gathered keys above and at the threshold
+    uint32_t seg_off = 0u;
+    for (int r = 0; r < int(ncta); ++r) {
+      const uint32_t n = sm.cnt_r[r];
+      if (r % kWarpsAll == warp) {
+        uint32_t gtc = 0u, eqc = 0u;
+        for (uint32_t i = lane; i < n; i += 32) {
+          const uint32_t kk = gk[seg_off + i];
+          gtc += kk > T ? 1u : 0u;
+          eqc += kk == T ? 1u : 0u;
+        }
+        gtc = __reduce_add_sync(0xffffffffu, gtc);
+        eqc = __reduce_add_sync(0xffffffffu, eqc);
+        if (lane == 0) {
+          sm.gt_r[r] = sm.above_r[r] + gtc;
+          sm.eq_r[r] = q > 0u ? eqc : 0u;
+        }
+      }
+      seg_off += (n + 3u) & ~3u;
+    }
   }
+  __syncthreads();
 
-  // ---------------- phase 3: this CTA's quota, offset and ordered output
-  // Each thread owns a contiguous run of local positions so that a block scan
-  // in thread order is a scan in position order.
-  const int per_thread = (rows_total + kThreads - 1) / kThreads;
-  const int r0 = min(rows_total, tid * per_thread);
-  const int r1 = min(rows_total, r0 + per_thread);
-  uint32_t n_gt = 0u, n_eq = 0u;
-  for (int j0 = r0; j0 < r1; j0 += 8) {
-    uint32_t kk[8];
-#pragma unroll
-    for (int u = 0; u < 8; ++u) kk[u] = j0 + u < r1 ? s_key[j0 + u] : 0u;
-#pragma unroll
-    for (int u = 0; u < 8; ++u) {
-      if (kk[u] == 0u) continue;
-      if (take_all || kk[u] > T)
-        ++n_gt;
-      else if (kk[u] == T)
-        ++n_eq;
-    }
-  }
+  // Let the next launch in the stream start its CTAs only now: CTAs of the next
+  // kernel made resident earlier would sit on SM resources through this
+  // kernel's selection and slow its last clusters (measured: +12 us per step).
+  pdl_launch_dependents();
+
+  // ---------------- phase 3: this CTA's quota and offset, then its ids in ascending order
+  uint32_t offset = 0u, quota = 0u;
   {
-    uint32_t g = n_gt, e = n_eq;
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) {
-      g += __shfl_xor_sync(0xffffffffu, g, o);
-      e += __shfl_xor_sync(0xffffffffu, e, o);
+    uint32_t eqb = 0u;
+    for (int r = 0; r < int(ncta); ++r) {
+      const uint32_t qr = min(sm.eq_r[r], q > eqb ? q - eqb : 0u);
+      if (r < int(crank)) offset += sm.gt_r[r] + qr;
+      if (r == int(crank)) quota = qr;
+      eqb += sm.eq_r[r];
     }
-    if (lane == 0) {
-      sm.red[0][warp] = g;
-      sm.red[1][warp] = e;
-    }
-    __syncthreads();
-    if (tid == 0) {
-      uint32_t gg = 0, ee = 0;
-      for (int w = 0; w < kWarpsAll; ++w) {
-        gg += sm.red[0][w];
-        ee += sm.red[1][w];
-      }
-      sm.fin[0] = gg;
-      sm.fin[1] = ee;
-    }
-    cluster_sync_all();
-    if (tid == 0) {
-      uint32_t rg[kMaxCluster], re[kMaxCluster];
-#pragma unroll
-      for (int r = 0; r < kMaxCluster; ++r) {
-        rg[r] = r < int(crank) ? __float_as_uint(dsmem_ld_f32(dsmem_addr(&sm.fin[0], r))) : 0u;
-        re[r] = r < int(crank) ? __float_as_uint(dsmem_ld_f32(dsmem_addr(&sm.fin[1], r))) : 0u;
-      }
-      uint32_t off = 0, eq_before = 0;
-#pragma unroll
-      for (int r = 0; r < kMaxCluster; ++r) {
-        off += rg[r] + min(re[r], need_eq > eq_before ? need_eq - eq_before : 0u);
-        eq_before += re[r];
-      }
-      sm.offset = off;
-      sm.quota = min(sm.fin[1], need_eq > eq_before ? need_eq - eq_before : 0u);
-    }
-    __syncthreads();
   }
-  // exclusive block scan of (n_gt << 16 | n_eq) in thread order
-  uint32_t gt_before, eq_before;
-  {
-    const uint32_t v = (n_gt << 16) | n_eq;
-    uint32_t x = v;
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-      const uint32_t y = __shfl_up_sync(0xffffffffu, x, o);
-      if (lane >= o) x += y;
-    }
-    if (lane == 31) sm.red[2][warp] = x;
-    __syncthreads();
-    uint32_t pre = 0u;
-    for (int w = 0; w < warp; ++w) pre += sm.red[2][w];
-    const uint32_t ex = pre + x - v;
-    gt_before = ex >> 16;
-    eq_before = ex & 0xffffu;
+  // each warp owns a contiguous run of positions; ballots give the ranks inside it
+  const int seg = ((rows_total + kWarpsAll - 1) / kWarpsAll + 31) & ~31;
+  const int p0 = warp * seg;
+  const int p1 = min(rows_total, p0 + seg);
+  uint32_t wgt = 0u, weq = 0u;
+  for (int j0 = p0; j0 < p1; j0 += 32) {
+    const int j = j0 + lane;
+    const uint32_t kk = j < p1 ? s_key[j] : 0u;
+    wgt += uint32_t(__popc(__ballot_sync(0xffffffffu, kk > T)));
+    weq += uint32_t(__popc(__ballot_sync(0xffffffffu, q > 0u && kk == T)));
   }
-  const uint32_t quota = sm.quota;
-  uint32_t slot = sm.offset + gt_before + min(eq_before, quota);
+  if (lane == 0) {
+    sm.red[0][warp] = wgt;
+    sm.red[1][warp] = weq;
+  }
+  __syncthreads();
+  uint32_t gt_before = 0u, eq_before = 0u;
+  for (int w = 0; w < warp; ++w) {
+    gt_before += sm.red[0][w];
+    eq_before += sm.red[1][w];
+  }
+  uint32_t slot = offset + gt_before + min(eq_before, quota);
   int* out = a.out + (long long)b * a.ld_out;
-  for (int j0 = r0; j0 < r1; j0 += 8) {
-    uint32_t kk[8];
-#pragma unroll
-    for (int u = 0; u < 8; ++u) kk[u] = j0 + u < r1 ? s_key[j0 + u] : 0u;
-#pragma unroll
-    for (int u = 0; u < 8; ++u) {
-      if (kk[u] == 0u) continue;
-      bool take = false;
-      if (take_all || kk[u] > T) {
-        take = true;
-      } else if (kk[u] == T) {
-        take = eq_before < quota;
-        ++eq_before;
-      }
-      if (take) {
-        const int j = j0 + u;
-        int id;
-        if (!POOLED)
-          id = begin + j;
-        else
-          id = s_pool[j / kBlock] * kBlock + j % kBlock;
-        out[slot++] = id;
-      }
+  const unsigned lt = (1u << lane) - 1u;
+  for (int j0 = p0; j0 < p1; j0 += 32) {
+    const int j = j0 + lane;
+    const uint32_t kk = j < p1 ? s_key[j] : 0u;
+    const bool eq = q > 0u && kk == T;
+    const unsigned me = __ballot_sync(0xffffffffu, eq);
+    const bool take = kk > T || (eq && eq_before + uint32_t(__popc(me & lt)) < quota);
+    const unsigned mt = __ballot_sync(0xffffffffu, take);
+    if (take) {
+      int id;
+      if (!POOLED)
+        id = begin + j;
+      else
+        id = s_pool[j / kBlock] * kBlock + j % kBlock;
+      out[slot + uint32_t(__popc(mt & lt))] = id;
     }
+    slot += uint32_t(__popc(mt));
+    eq_before += uint32_t(__popc(me));
   }
-  const int selected = int(min(n_sel_valid, k));
+  const int selected = int(min(n_all, k));
   if (crank == 0) {
     if (a.n_out != nullptr && tid == 0) a.n_out[b] = selected;
     for (int j = selected + tid; j < a.k; j += kThreads) out[j] = -1;
   }
-  cluster_sync_all();   // no CTA leaves while another may still read its shared memory
 }
 
 struct ClusterChoice {
