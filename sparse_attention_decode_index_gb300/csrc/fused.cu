@@ -130,9 +130,12 @@ __device__ __forceinline__ uint32_t bin_of(uint32_t key, const Binning& bn) {
 constexpr size_t kOffSmall = size_t(kStages) * kTileBytes;
 constexpr size_t kOffKeys = kOffSmall + ((sizeof(SelSmall) + 127) / 128) * 128;
 
+// Keys are stored in a multiple of 4 words so that 16-byte reads stay inside them.
+__host__ __device__ constexpr int key_words(int rows) { return (rows + 3) & ~3; }
+
 size_t select_smem_bytes(int rows_per_cta, bool pooled) {
   const int rows = pooled ? rows_per_cta * kBlock : rows_per_cta;
-  return kOffKeys + size_t(rows) * 4 + (pooled ? size_t(rows_per_cta) * 4 : 0);
+  return kOffKeys + size_t(key_words(rows)) * 4 + (pooled ? size_t(rows_per_cta) * 4 : 0);
 }
 
 template <bool POOLED>
@@ -142,7 +145,7 @@ __global__ void __launch_bounds__(kThreads, 4) index_select_kernel(const SelectA
   SelSmall& sm = *reinterpret_cast<SelSmall*>(smem + kOffSmall);
   uint32_t* s_key = reinterpret_cast<uint32_t*>(smem + kOffKeys);
   const int units_cap = a.rows_per_cta;                                 // rows (flat) or blocks (pooled)
-  int* s_pool = reinterpret_cast<int*>(s_key + (POOLED ? units_cap * kBlock : units_cap));
+  int* s_pool = reinterpret_cast<int*>(s_key + key_words(POOLED ? units_cap * kBlock : units_cap));
 
   const int b = blockIdx.y;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -410,8 +413,10 @@ __global__ void __launch_bounds__(kThreads, 4) index_select_kernel(const SelectA
       for (int r = 0; r < int(ncta); ++r) dsmem_st_v2u(dsmem_addr(dst, uint32_t(r)), sum & 0xffffu, sum >> 16);
     }
     cluster_sync_all();
-    if (warp == 0) {
-      // lane l holds bins 255 - 8l - j (j = 0..7); first their totals over the CTAs
+    uint32_t sel, sabove;
+    {
+      // Every warp finds the bin (same data, same result); lane l holds bins
+      // 255 - 8l - j (j = 0..7), first their totals over the CTAs.
       const uint32_t* tb = tot + buf * kTotWords;
       const int b0 = kBins - 8 - 8 * lane;
       uint32_t g[8] = {0u, 0u, 0u, 0u, 0u, 0u, 0u, 0u};
@@ -444,10 +449,11 @@ __global__ void __launch_bounds__(kThreads, 4) index_select_kernel(const SelectA
       const unsigned fm = __ballot_sync(0xffffffffu, fj >= 0);
       const int fl = fm ? __ffs(fm) - 1 : 0;
       const int sj = max(0, __shfl_sync(0xffffffffu, fj, fl));
-      const uint32_t sabove = __shfl_sync(0xffffffffu, fabove, fl);
-      const uint32_t sel = uint32_t(kBins - 1 - 8 * fl - sj);
-      // then each CTA's keys above the chosen bin and inside it
-      for (int r = 0; r < int(ncta); ++r) {
+      sabove = __shfl_sync(0xffffffffu, fabove, fl);
+      sel = uint32_t(kBins - 1 - 8 * fl - sj);
+      if (fm == 0u && tid == 0) report(a.err, kErrBadCount, -2);   // cannot happen: [lo, hi] holds >= need keys
+      // then each CTA's keys above the chosen bin and inside it (CTA r by warp r mod 5)
+      for (int r = warp; r < int(ncta); r += kWarpsAll) {
         const uint4 x = *reinterpret_cast<const uint4*>(tb + r * kBins + b0);
         const uint4 y = *reinterpret_cast<const uint4*>(tb + r * kBins + b0 + 4);
         const uint32_t v[8] = {x.x, x.y, x.z, x.w, y.x, y.y, y.z, y.w};   // bins b0 .. b0 + 7
@@ -465,16 +471,11 @@ __global__ void __launch_bounds__(kThreads, 4) index_select_kernel(const SelectA
           sm.cnt_r[r] = in;
         }
       }
-      if (lane == 0) {
-        sm.sel_bin = sel;
-        sm.sel_above = sabove;
-        if (fm == 0u) report(a.err, kErrBadCount, -2);   // cannot happen: [lo, hi] holds >= need keys
-      }
     }
     __syncthreads();
-    need -= sm.sel_above;
+    need -= sabove;
     flt = bn;
-    fsel = sm.sel_bin;
+    fsel = sel;
     filtered = true;
     uint32_t padded = 0u;
     for (int r = 0; r < int(ncta); ++r) padded += (sm.cnt_r[r] + 3u) & ~3u;
@@ -493,17 +494,16 @@ __global__ void __launch_bounds__(kThreads, 4) index_select_kernel(const SelectA
       G += (sm.cnt_r[r] + 3u) & ~3u;
     }
     const uint32_t my_in = sm.cnt_r[crank];
-    for (int j0 = warp * 32; j0 < rows_total; j0 += kThreads) {
-      const int j = j0 + lane;
-      const uint32_t kk = j < rows_total ? s_key[j] : 0u;
-      const bool in = kk != 0u && kk >= lo && kk <= hi && bin_of(kk, flt) == fsel;
-      const unsigned m = __ballot_sync(0xffffffffu, in);
-      if (m != 0u) {
-        uint32_t base = 0u;
-        if (lane == 0) base = atomicAdd(&sm.gcount, uint32_t(__popc(m)));
-        base = __shfl_sync(0xffffffffu, base, 0);
-        if (in) gk[my_off + base + uint32_t(__popc(m & ((1u << lane) - 1u)))] = kk;
-      }
+    for (int j0 = tid; j0 < rows_total; j0 += 8 * kThreads) {   // few keys match: one atomic each
+      uint32_t kk[8];
+#pragma unroll
+      for (int u = 0; u < 8; ++u) kk[u] = j0 + u * kThreads < rows_total ? s_key[j0 + u * kThreads] : 0u;
+#pragma unroll
+      for (int u = 0; u < 8; ++u)
+        if (kk[u] != 0u && kk[u] >= lo && kk[u] <= hi && bin_of(kk[u], flt) == fsel) {
+          const uint32_t p = atomicAdd(&sm.gcount, 1u);
+          if (p < my_in) gk[my_off + p] = kk[u];
+        }
     }
     if (tid < 3 && my_in + uint32_t(tid) < ((my_in + 3u) & ~3u)) gk[my_off + my_in + tid] = 0u;
     __syncthreads();
