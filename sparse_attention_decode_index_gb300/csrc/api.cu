@@ -29,11 +29,12 @@ int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
 
 struct WsLayout {
   size_t hdr, pool, n_pool, n_blk, blk_scores, tok_scores, tok_cand, n_cand, tk_ids_a, tk_sc_a, tk_ids_b,
-      tk_sc_b, idx, total;
+      tk_sc_b, idx, attn_part, total;
   int64_t nb_cap, tok_ld, tk_chunks, tk_kmax;
 };
 
 bool hier_possible(const csa2_shape& s) { return s.pool_blocks > 0; }
+bool attn_fast(const csa2_shape& s);
 
 WsLayout layout(const csa2_shape& s) {
   WsLayout L{};
@@ -65,6 +66,9 @@ WsLayout layout(const csa2_shape& s) {
   L.tk_ids_b = take(tk);
   L.tk_sc_b = take(tk);
   L.idx = take(size_t(B) * s.topk * 4);
+  // fast attention: every CTA of a query's cluster leaves its partial O of all heads here
+  const int64_t attn_c = attn_fast(s) ? attn_cluster(s.topk, s.swa) : 0;
+  L.attn_part = take(size_t(B * attn_c * s.q_heads * s.v_dim) * 4);
   L.total = off;
   return L;
 }
@@ -98,7 +102,7 @@ bool indexer_fast(const csa2_shape& s) { return s.dtype == CSA2_BF16 && s.idx_he
 bool pooled_fast(const csa2_shape& s) { return indexer_fast(s) && s.block == 8; }
 bool attn_fast(const csa2_shape& s) {
   return s.dtype == CSA2_BF16 && s.q_heads == 64 && s.k_dim == 192 && s.v_dim == 128 &&
-         ceil_div(s.topk + s.swa, attn_slots_per_cta()) <= attn_max_cluster();
+         attn_cluster(s.topk, s.swa) > 0;
 }
 
 int check_ws(const csa2_shape& s, void* ws, size_t bytes) {
@@ -218,7 +222,7 @@ int do_topk(const csa2_shape& s, const WsLayout& L, void* ws, const float* score
 
 int do_attn(const csa2_shape& s, const void* q, const void* k_main, const void* v_main, const int32_t* idx,
             const void* k_swa, const void* v_swa, const int32_t* n_swa, float* out, float* lse, int* err,
-            cudaStream_t st, bool swa_only = false) {
+            float* part, cudaStream_t st, bool swa_only = false) {
   AttnArgs a{};
   a.q = q;
   a.k_main = k_main;
@@ -237,6 +241,7 @@ int do_attn(const csa2_shape& s, const void* q, const void* k_main, const void* 
   a.v_dim = s.v_dim;
   a.dtype = s.dtype;
   a.scale = softmax_scale(s);
+  a.part = part;
   a.err = err;
   return cuda_status(launch_attn(a, attn_fast(s), s.batch, st));
 }
@@ -431,7 +436,8 @@ int csa2_sparse_attn(const csa2_shape* shape, const void* q, const void* k_main,
   CSA2_TRY(check_attn_args(s, q, k_main, v_main, out));
   CSA2_TRY(check_sswa(s, k_swa, v_swa, n_swa));
   const WsLayout L = layout(s);
-  return do_attn(s, q, k_main, v_main, idx, k_swa, v_swa, n_swa, out, lse, at<int>(ws, L.hdr), stream);
+  return do_attn(s, q, k_main, v_main, idx, k_swa, v_swa, n_swa, out, lse, at<int>(ws, L.hdr),
+                 at<float>(ws, L.attn_part), stream);
 }
 
 int csa2_layer_group(const csa2_shape* shape, const csa2_layer* layers, int32_t n_layers, const void* k_main,
@@ -472,7 +478,8 @@ int csa2_layer_group(const csa2_shape* shape, const csa2_layer* layers, int32_t 
   for (int l = 0; l < n_layers; ++l) {
     const csa2_layer& y = layers[l];
     if (y.mode == CSA2_SWA) {
-      CSA2_TRY(do_attn(s, y.q, k_main, v_main, nullptr, y.k_swa, y.v_swa, n_swa, y.out, y.lse, err, stream, true));
+      CSA2_TRY(do_attn(s, y.q, k_main, v_main, nullptr, y.k_swa, y.v_swa, n_swa, y.out, y.lse, err,
+                     at<float>(ws, L.attn_part), stream, true));
       continue;
     }
     if (y.mode != CSA2_REUSE) {
@@ -510,7 +517,8 @@ int csa2_layer_group(const csa2_shape* shape, const csa2_layer* layers, int32_t 
       }
       cur = dst;
     }
-    CSA2_TRY(do_attn(s, y.q, k_main, v_main, cur, y.k_swa, y.v_swa, n_swa, y.out, y.lse, err, stream));
+    CSA2_TRY(do_attn(s, y.q, k_main, v_main, cur, y.k_swa, y.v_swa, n_swa, y.out, y.lse, err,
+                     at<float>(ws, L.attn_part), stream));
   }
   return CSA2_OK;
 }

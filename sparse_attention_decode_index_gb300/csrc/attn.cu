@@ -6,24 +6,33 @@
 // with cross-layer reuse": every mode computes its own main Q and SWA KV).
 //
 // Fast path (bf16, 64 heads sharing one KV head, dk 192, dv 128): the
-// 512 + 128 key slots of one query are split over a thread-block cluster of
-// ceil(slots / 160) CTAs (4 for the architecture's 640 slots), sized so that two
-// CTAs fit per SM and every cluster of a 64-query batch is resident in one wave.
-// Each CTA gathers its 160 K rows (384 B) and V rows (256 B) into padded
-// shared-memory rows with 16-byte cp.async copies -- consecutive threads copy
-// consecutive 16-byte pieces of one row, so every row is read contiguously --
-// in two commit groups (slots 0..79, 80..159) so the first half of the keys
-// can be scored while the second is still arriving.  (Per-row bulk copies were
+// 512 + 128 key slots of one query are split over a thread-block cluster of C
+// CTAs (4 for the architecture's 640 slots), sized so that two CTAs fit per SM
+// and every cluster of a 64-query batch is resident in one wave.  CTA c holds
+// SWA rows [c * sp, (c + 1) * sp) in its first local slots and main index slots
+// [c * mp, (c + 1) * mp) after them (mp = ceil(topk / C), sp = ceil(swa / C),
+// mp + sp <= 160).  The SWA rows are inputs of the launch, so every CTA starts
+// fetching them before it waits for the preceding launch to finish.
+// Each CTA gathers its K rows (384 B) and V rows (256 B) into padded
+// shared-memory rows with 16-byte cp.async copies: a warp copies one slot at a
+// time, lane l taking the fixed 16-byte pieces l and l + 32 of the slot's 640
+// bytes, so every row is read contiguously.  Three commit groups (SWA rows,
+// then local slots below 80, then the rest) let the first half of the keys be
+// scored while the second is still arriving.  (Per-row bulk copies were
 // measured to be limited by the rate at which the TMA unit accepts small
-// copies.)  Invalid slots (index -1, or beyond n_swa) are zero-filled by the
-// copies themselves and masked.  Four warps each own 16 heads; their Q fragments are loaded straight
-// into registers while the gather is in flight.  S = Q K^T and O = P V run on
+// copies.)  Invalid slots (index -1, beyond n_swa, or unused) are zero-filled
+// by the copies themselves and masked.  Four warps each own 16 heads; their Q
+// fragments are loaded straight into registers while the gather is in flight.  S = Q K^T and O = P V run on
 // mma.sync m16n8k16 (bf16 in, fp32 accumulate) with a base-2 fp32 softmax.
-// The partials of the cluster are merged through distributed shared memory
-// with remote stores only: every CTA writes its per-head (m, l) into every
-// CTA, scales its own partial O by exp2(m_c - M) / L and pushes it to the CTA
-// that owns those heads, which sums the pushed partials in fixed CTA order.
-// No partial touches global memory and the result is deterministic.
+// The partials of the cluster are merged with a single cluster barrier: every
+// CTA pushes its per-head (m, l) into the table of the CTA that owns those
+// heads (distributed shared memory) and writes its unscaled partial O, as
+// 16-byte vectors assembled from lane pairs, to workspace scratch that stays
+// in L2; the owner then weights the partials by exp2(m_c - M) / L and sums them
+// in fixed CTA order, so the result is deterministic.  (Pushing the partials
+// through distributed shared memory instead needs a second barrier -- they
+// would land in the K region while a peer may still be reading it -- and was
+// measured slower.)
 #include "common.cuh"
 #include "internal.h"
 
@@ -37,7 +46,6 @@ constexpr int kNT = kSlots / 8;                   // S n-tiles (8 keys each)
 constexpr int kThreads = 128;
 constexpr int kKRow = kDk * 2 + 16;               // 400 B: padded so ldmatrix rows hit distinct banks
 constexpr int kVRow = kDv * 2 + 16;               // 272 B
-constexpr int kORow = kDv + 4;                    // fp32 partial O row (floats), 16 B multiple
 constexpr int kMaxCluster = 8;
 
 constexpr int kOffK = 0;
@@ -45,11 +53,8 @@ constexpr int kOffV = kOffK + kSlots * kKRow;     // 64,000
 constexpr int kOffM = kOffV + kSlots * kVRow;     // 107,520: [kMaxCluster][kH] m of every CTA
 constexpr int kOffL = kOffM + kMaxCluster * kH * 4;   // [kMaxCluster][kH] l of every CTA
 constexpr int kOffValid = kOffL + kMaxCluster * kH * 4;
-constexpr int kOffSrc = kOffValid + kSlots * 4;            // [kSlots] K row, then [kSlots] V row addresses
-constexpr int kSmemBytes = kOffSrc + 2 * kSlots * 8;
+constexpr int kSmemBytes = kOffValid + kSlots * 4;
 constexpr int kHalf = kSlots / 2;                 // slots per gather barrier (80)
-// pushed partials: [ncta][ceil(kH / ncta)][kDv] floats in the (dead) K region
-static_assert((kH + kMaxCluster - 1) * kDv * 4 <= kSlots * kKRow, "pushed partials must fit in the K region");
 static_assert(kSlots % 16 == 0, "PV k-steps need 16-key groups");
 static_assert(kNT % 4 == 0, "each gather half covers whole n-tile pairs");
 
@@ -60,9 +65,6 @@ __global__ void __launch_bounds__(kThreads, 2) attn_mma_kernel(const AttnArgs a)
   float* sM = reinterpret_cast<float*>(smem + kOffM);
   float* sL = reinterpret_cast<float*>(smem + kOffL);
   int* sValid = reinterpret_cast<int*>(smem + kOffValid);
-  const uint8_t** sKsrc = reinterpret_cast<const uint8_t**>(smem + kOffSrc);
-  const uint8_t** sVsrc = sKsrc + kSlots;
-  float* sRecv = reinterpret_cast<float*>(smem + kOffK);   // pushed partials, after S and PV everywhere
 
   const int b = blockIdx.y;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -70,6 +72,53 @@ __global__ void __launch_bounds__(kThreads, 2) attn_mma_kernel(const AttnArgs a)
   const uint32_t crank = cluster_rank(), ncta = cluster_size();
 
   pdl_launch_dependents();
+  const int mp = (a.topk + int(ncta) - 1) / int(ncta);   // main index slots of this CTA
+  const int sp = (a.swa + int(ncta) - 1) / int(ncta);    // SWA rows of this CTA (local slots first)
+
+  // Slots are copied four at a time: the 4 x 40 16-byte pieces of four
+  // consecutive slots (K row: pieces 0..23, V row: 24..39 of each) are 5
+  // full-warp cp.async instructions; instruction k of lane l copies piece
+  // 32k + l, i.e. slot (32k + l) / 40 of the four, piece (32k + l) % 40.
+  const uint8_t* zsrc = static_cast<const uint8_t*>(a.k_main);   // any valid address (0 bytes read)
+  int q_slot[5], q_off[5], q_dst[5];
+  bool q_k[5];
+#pragma unroll
+  for (int k = 0; k < 5; ++k) {
+    const int p = 32 * k + lane;
+    const int part = p % 40;
+    q_slot[k] = p / 40;
+    q_k[k] = part < 24;
+    q_off[k] = q_k[k] ? part * 16 : (part - 24) * 16;
+    q_dst[k] = q_slot[k] * (q_k[k] ? kKRow : kVRow) + q_off[k];
+  }
+  // Copy slots [ls0, ls0 + 4); lane j (j < 4) supplies slot ls0 + j's K and V rows (null: zero fill).
+  auto copy_quad = [&](int ls0, const uint8_t* krow, const uint8_t* vrow) {
+#pragma unroll
+    for (int k = 0; k < 5; ++k) {
+      const uint8_t* kr = reinterpret_cast<const uint8_t*>(__shfl_sync(0xffffffffu, reinterpret_cast<uintptr_t>(krow), q_slot[k]));
+      const uint8_t* vr = reinterpret_cast<const uint8_t*>(__shfl_sync(0xffffffffu, reinterpret_cast<uintptr_t>(vrow), q_slot[k]));
+      const uint8_t* r = q_k[k] ? kr : vr;
+      uint8_t* d = (q_k[k] ? sK + ls0 * kKRow : sV + ls0 * kVRow) + q_dst[k];
+      asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(smem_u32(d)),
+                   "l"(r != nullptr ? r + q_off[k] : zsrc), "r"(r != nullptr ? 16u : 0u)
+                   : "memory");
+    }
+  };
+
+  // --- group 0: this CTA's SWA rows (inputs of this launch), before waiting on the preceding one.
+  // Local slots are handled in quads [4m, 4m + 4), quad m by warp m mod 4.
+  const int ns = clamp_count(a.n_swa[b], a.swa, a.err);
+  for (int q0 = 4 * warp; q0 < (sp & ~3); q0 += 16) {
+    const int ls = q0 + (lane & 3);
+    const int r = int(crank) * sp + ls;
+    const bool ok = lane < 4 && r < a.swa && r < ns;
+    const long long row = (long long)b * a.swa + r;
+    copy_quad(q0, ok ? static_cast<const uint8_t*>(a.k_swa) + row * (kDk * 2) : nullptr,
+              ok ? static_cast<const uint8_t*>(a.v_swa) + row * (kDv * 2) : nullptr);
+    if (lane < 4) sValid[ls] = ok ? 1 : 0;
+  }
+  asm volatile("cp.async.commit_group;" ::: "memory");
+
   // --- Q A-fragments for heads 16w + g and 16w + g + 8, straight from global
   uint32_t qa[kDk / 16][4];
   {
@@ -86,46 +135,46 @@ __global__ void __launch_bounds__(kThreads, 2) attn_mma_kernel(const AttnArgs a)
   }
   pdl_wait();   // the indices come from the preceding launch
 
-  // --- source rows of this CTA's 160 key slots (null: invalid slot)
-  const int ns = clamp_count(a.n_swa[b], a.swa, a.err);
-  for (int ls = tid; ls < kSlots; ls += kThreads) {
-    const int slot = blockIdx.x * kSlots + ls;
-    const uint8_t* ks = nullptr;
-    const uint8_t* vs = nullptr;
-    if (slot < a.topk) {
-      const int e = a.idx[(long long)b * a.topk + slot];
-      if (e >= a.n_entries) report(a.err, kErrBadIndex, e);
-      if (e >= 0 && e < a.n_entries) {
-        const long long r = (long long)b * a.n_entries + e;
-        ks = static_cast<const uint8_t*>(a.k_main) + r * (kDk * 2);
-        vs = static_cast<const uint8_t*>(a.v_main) + r * (kDv * 2);
-      }
-    } else if (slot < a.topk + a.swa && slot - a.topk < ns) {
-      const long long r = (long long)b * a.swa + (slot - a.topk);
-      ks = static_cast<const uint8_t*>(a.k_swa) + r * (kDk * 2);
-      vs = static_cast<const uint8_t*>(a.v_swa) + r * (kDv * 2);
-    }
-    sKsrc[ls] = ks;
-    sVsrc[ls] = vs;
-    sValid[ls] = ks != nullptr ? 1 : 0;
-  }
-  __syncthreads();
+  // --- main index of every slot of this warp's quads 4 * warp + 16i: lane l holds
+  // quad i = l / 4 (slot l % 4) in e0 and quad i = 8 + l / 4 in e1 (l < 8); -1: no main row
+  auto main_index = [&](int ls) -> int {
+    const int lm = ls - sp;
+    if (ls >= kSlots || lm < 0 || lm >= mp || int(crank) * mp + lm >= a.topk) return -1;
+    return a.idx[(long long)b * a.topk + int(crank) * mp + lm];
+  };
+  const int e0 = main_index(4 * warp + 16 * (lane >> 2) + (lane & 3));
+  const int e1 = lane < 8 ? main_index(4 * warp + 16 * (8 + (lane >> 2)) + (lane & 3)) : -1;
 
-  // --- gather: 16-byte pieces, 24 per K row and 16 per V row; two commit groups
-  constexpr int kPieces = (kDk * 2 + kDv * 2) / 16;        // 40 per slot
-  const uint8_t* zsrc = static_cast<const uint8_t*>(a.k_main);   // any valid address (0 bytes read)
-#pragma unroll
-  for (int half = 0; half < 2; ++half) {
-    for (int c = tid; c < kHalf * kPieces; c += kThreads) {
-      const int ls = half * kHalf + c / kPieces, part = c % kPieces;
-      const bool isk = part < (kDk * 2) / 16;
-      const uint8_t* row = isk ? sKsrc[ls] : sVsrc[ls];
-      const int off = isk ? part * 16 : (part - (kDk * 2) / 16) * 16;
-      uint8_t* dst = isk ? sK + ls * kKRow + off : sV + ls * kVRow + off;
-      const uint32_t n = row != nullptr ? 16u : 0u;          // 0 source bytes: zero fill
-      asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(smem_u32(dst)),
-                   "l"(row != nullptr ? row + off : zsrc), "r"(n)
-                   : "memory");
+  // --- groups 1 and 2: the remaining quads (main rows, the last partial SWA quad, unused slots),
+  // below / from local slot 80.  Lane j < 4 of a quad resolves slot q0 + j.
+  const int first = sp & ~3;
+#pragma unroll 1
+  for (int grp = 1; grp <= 2; ++grp) {
+    const int lo = grp == 1 ? first : max(first, kHalf), hi = grp == 1 ? max(first, kHalf) : kSlots;
+    for (int q0 = lo + ((4 * warp - lo) & 15); q0 < hi; q0 += 16) {
+      const int ls = q0 + (lane & 3);
+      const int qi = (q0 - 4 * warp) >> 4;
+      const int e = __shfl_sync(0xffffffffu, qi < 8 ? e0 : e1, ((qi & 7) << 2) | (lane & 3));
+      const uint8_t* kr = nullptr;
+      const uint8_t* vr = nullptr;
+      bool ok = false;
+      if (lane < 4) {
+        if (ls < sp) {
+          const int r = int(crank) * sp + ls;
+          ok = r < a.swa && r < ns;
+          const long long row = (long long)b * a.swa + r;
+          kr = static_cast<const uint8_t*>(a.k_swa) + row * (kDk * 2);
+          vr = static_cast<const uint8_t*>(a.v_swa) + row * (kDv * 2);
+        } else {
+          if (e >= a.n_entries) report(a.err, kErrBadIndex, e);
+          ok = e >= 0 && e < a.n_entries;
+          const long long row = (long long)b * a.n_entries + e;
+          kr = static_cast<const uint8_t*>(a.k_main) + row * (kDk * 2);
+          vr = static_cast<const uint8_t*>(a.v_main) + row * (kDv * 2);
+        }
+        sValid[ls] = ok ? 1 : 0;
+      }
+      copy_quad(q0, ok ? kr : nullptr, ok ? vr : nullptr);
     }
     asm volatile("cp.async.commit_group;" ::: "memory");
   }
@@ -138,7 +187,7 @@ __global__ void __launch_bounds__(kThreads, 2) attn_mma_kernel(const AttnArgs a)
 #pragma unroll
   for (int half = 0; half < 2; ++half) {
     if (half == 0)
-      asm volatile("cp.async.wait_group 1;" ::: "memory");
+      asm volatile("cp.async.wait_group 1;" ::: "memory");   // groups 0 and 1: local slots below 80
     else
       asm volatile("cp.async.wait_group 0;" ::: "memory");
     __syncthreads();
@@ -208,60 +257,71 @@ __global__ void __launch_bounds__(kThreads, 2) attn_mma_kernel(const AttnArgs a)
     }
   }
 
-  // --- merge across the cluster (remote stores only)
+  // --- merge across the cluster, one barrier: every CTA pushes the (m, l) of
+  // its rows into the table of the CTA that owns those heads and writes its
+  // unscaled partial O of all heads to global scratch (L2); after the barrier
+  // the owner weights the partials by exp2(m_c - M) and sums them in fixed
+  // CTA order.
   const int h0 = warp * 16 + g, h1 = h0 + 8;
-  // 1. every CTA's (m, l) of every head into every CTA: table [rank][head]
-  if (t == 0) {
-    for (uint32_t r = 0; r < ncta; ++r) {
-      dsmem_st_f32(dsmem_addr(sM + crank * kH + h0, r), m0);
-      dsmem_st_f32(dsmem_addr(sL + crank * kH + h0, r), l0);
-      dsmem_st_f32(dsmem_addr(sM + crank * kH + h1, r), m1);
-      dsmem_st_f32(dsmem_addr(sL + crank * kH + h1, r), l1);
-    }
-  }
-  cluster_sync_all();   // tables complete; every CTA is past its S and PV (K/V regions free)
-  // 2. own factor exp2(m_own - M) / L for rows h0, h1; scale and push to the head's owner
   const int per_owner = (kH + int(ncta) - 1) / int(ncta);
-  float f0 = 0.f, f1 = 0.f;
-  {
-    float M0 = -INFINITY, M1 = -INFINITY;
-    for (uint32_t r = 0; r < ncta; ++r) {
-      M0 = fmaxf(M0, sM[r * kH + h0]);
-      M1 = fmaxf(M1, sM[r * kH + h1]);
-    }
-    float L0 = 0.f, L1 = 0.f;
-    for (uint32_t r = 0; r < ncta; ++r) {
-      const float a0 = sM[r * kH + h0], a1 = sM[r * kH + h1];
-      if (a0 != -INFINITY) L0 += exp2f(a0 - M0) * sL[r * kH + h0];
-      if (a1 != -INFINITY) L1 += exp2f(a1 - M1) * sL[r * kH + h1];
-    }
-    if (M0 != -INFINITY && m0 != -INFINITY) f0 = exp2f(m0 - M0) / L0;
-    if (M1 != -INFINITY && m1 != -INFINITY) f1 = exp2f(m1 - M1) / L1;
+  if (t == 0) {
+    const uint32_t own0 = uint32_t(h0 / per_owner), own1 = uint32_t(h1 / per_owner);
+    dsmem_st_f32(dsmem_addr(sM + crank * kH + h0, own0), m0);
+    dsmem_st_f32(dsmem_addr(sL + crank * kH + h0, own0), l0);
+    dsmem_st_f32(dsmem_addr(sM + crank * kH + h1, own1), m1);
+    dsmem_st_f32(dsmem_addr(sL + crank * kH + h1, own1), l1);
   }
   {
-    const uint32_t own0 = uint32_t(h0 / per_owner), own1 = uint32_t(h1 / per_owner);
-    float* dst0 = sRecv + ((size_t)crank * per_owner + (h0 - int(own0) * per_owner)) * kDv;
-    float* dst1 = sRecv + ((size_t)crank * per_owner + (h1 - int(own1) * per_owner)) * kDv;
+    // Lane pairs (t, t ^ 1) trade halves so that the even lane stores 4
+    // consecutive columns of row h0 and the odd lane 4 of row h1.
+    const bool even = (t & 1) == 0;
+    float* prow = a.part + ((size_t)(b * int(ncta) + int(crank)) * kH + (even ? h0 : h1)) * kDv;
 #pragma unroll
     for (int j = 0; j < kDv / 8; ++j) {
-      dsmem_st_v2(dsmem_addr(dst0 + 8 * j + 2 * t, own0), o[j][0] * f0, o[j][1] * f0);
-      dsmem_st_v2(dsmem_addr(dst1 + 8 * j + 2 * t, own1), o[j][2] * f1, o[j][3] * f1);
+      const float rx = __shfl_xor_sync(0xffffffffu, even ? o[j][2] : o[j][0], 1);
+      const float ry = __shfl_xor_sync(0xffffffffu, even ? o[j][3] : o[j][1], 1);
+      const int col = 8 * j + 2 * t - (even ? 0 : 2);
+      __stcg(reinterpret_cast<float4*>(prow + col),
+             even ? make_float4(o[j][0], o[j][1], rx, ry) : make_float4(rx, ry, o[j][2], o[j][3]));
     }
   }
-  cluster_sync_all();   // every pushed partial has landed in its owner
-  // 3. the owner sums its heads in CTA order and writes out / lse
+  cluster_sync_all();   // tables and partials of every CTA are complete and visible
+  // the owner sums its heads in CTA order (L2 loads: the partials come from other SMs);
+  // weights exp2(m_r - M) / L per (CTA, head) first, into the now unused K region
   const int hb = int(crank) * per_owner, he = min(kH, hb + per_owner);
-  for (int e = tid; e < (he - hb) * (kDv / 4); e += kThreads) {
-    const int hl = e / (kDv / 4), d4 = e % (kDv / 4);
-    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+  float* sW = reinterpret_cast<float*>(sK);   // [kMaxCluster][kH]
+  for (int h = hb + tid; h < he; h += kThreads) {
+    float M = -INFINITY;
+    for (uint32_t r = 0; r < ncta; ++r) M = fmaxf(M, sM[r * kH + h]);
+    float L = 0.f;
     for (uint32_t r = 0; r < ncta; ++r) {
-      const float4 v = *reinterpret_cast<const float4*>(sRecv + ((size_t)r * per_owner + hl) * kDv + 4 * d4);
-      acc.x += v.x;
-      acc.y += v.y;
-      acc.z += v.z;
-      acc.w += v.w;
+      const float mr = sM[r * kH + h];
+      const float wr = (M == -INFINITY || mr == -INFINITY) ? 0.f : exp2f(mr - M);
+      sW[r * kH + h] = wr;
+      L += wr * sL[r * kH + h];
     }
-    *reinterpret_cast<float4*>(a.out + ((long long)b * kH + hb + hl) * kDv + 4 * d4) = acc;
+    const float inv = L > 0.f ? 1.f / L : 0.f;
+    for (uint32_t r = 0; r < ncta; ++r) sW[r * kH + h] *= inv;
+  }
+  __syncthreads();
+  for (int e = tid; e < (he - hb) * (kDv / 4); e += kThreads) {
+    const int h = hb + e / (kDv / 4), d4 = e % (kDv / 4);
+    float4 v[kMaxCluster];
+#pragma unroll
+    for (int r = 0; r < kMaxCluster; ++r)
+      if (r < int(ncta))
+        v[r] = __ldcg(reinterpret_cast<const float4*>(a.part + ((size_t)(b * int(ncta) + r) * kH + h) * kDv + 4 * d4));
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+    for (int r = 0; r < kMaxCluster; ++r)
+      if (r < int(ncta)) {
+        const float wr = sW[r * kH + h];
+        acc.x += wr * v[r].x;
+        acc.y += wr * v[r].y;
+        acc.z += wr * v[r].z;
+        acc.w += wr * v[r].w;
+      }
+    *reinterpret_cast<float4*>(a.out + ((long long)b * kH + h) * kDv + 4 * d4) = acc;
   }
   if (a.lse != nullptr && tid < he - hb) {
     const int h = hb + tid;
@@ -367,13 +427,19 @@ cudaError_t launch_attn(const AttnArgs& a, bool fast, int batch, cudaStream_t st
     if (e != cudaSuccess) return e;
     attr_set = true;
   }
-  const int ncta = (a.topk + a.swa + kSlots - 1) / kSlots;
+  const int ncta = attn_cluster(a.topk, a.swa);
+  if (ncta == 0) return cudaErrorInvalidValue;
   note_launch();
   return launch_pdl(attn_mma_kernel, dim3(unsigned(ncta), unsigned(batch), 1), dim3(kThreads), kSmemBytes, st,
                     unsigned(ncta), a);
 }
 
-int attn_max_cluster() { return kMaxCluster; }
-int attn_slots_per_cta() { return kSlots; }
+// Smallest cluster whose CTAs can each hold ceil(topk / C) main and
+// ceil(swa / C) SWA slots; 0 when no cluster of at most kMaxCluster can.
+int attn_cluster(int topk, int swa) {
+  for (int c = (topk + swa + kSlots - 1) / kSlots; c <= kMaxCluster; ++c)
+    if (c >= 1 && (topk + c - 1) / c + (swa + c - 1) / c <= kSlots) return c;
+  return 0;
+}
 
 }  // namespace csa2

@@ -191,6 +191,12 @@ CSA2_DEV void dsmem_st_v4u(uint32_t addr, uint4 v) {
                : "memory");
 }
 
+CSA2_DEV void dsmem_st_v4f(uint32_t addr, float4 v) {
+  asm volatile("st.shared::cluster.v4.f32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "f"(v.x), "f"(v.y), "f"(v.z),
+               "f"(v.w)
+               : "memory");
+}
+
 CSA2_DEV float dsmem_ld_f32(uint32_t addr) {
   float v;
   asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(addr) : "memory");

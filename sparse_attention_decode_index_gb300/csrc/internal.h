@@ -64,6 +64,7 @@ struct AttnArgs {
   int n_entries, topk, swa;
   int heads, k_dim, v_dim, dtype;
   float scale;               // softmax scale (natural-log domain)
+  float* part;               // fast path: [B, cluster, H, dv] fp32 partials (workspace scratch)
   int* err;
 };
 
@@ -141,8 +142,8 @@ int topk_max_chunk();
 // Cluster Top-k over one row of up to topk_cluster_max() positions (one launch).
 cudaError_t launch_topk_cluster(const TopkArgs& a, int batch, cudaStream_t st);
 int topk_cluster_max();
-int attn_max_cluster();
-int attn_slots_per_cta();
+// Cluster size of the fast attention kernel for these slot counts (0: unsupported).
+int attn_cluster(int topk, int swa);
 // fast: bf16, 64 heads, dk 192, dv 128
 cudaError_t launch_attn(const AttnArgs& a, bool fast, int batch, cudaStream_t st);
 
