@@ -36,6 +36,14 @@
  *     clamped or skipped by the kernels and recorded in a sticky error word in
  *     the workspace header; kernels never trap.  Read it with
  *     csa2_read_device_error.
+ *   - Kernels are launched with programmatic dependent launch.  Some read
+ *     the call's own inputs (q, SWA rows, n_swa, k_swa, v_swa) before waiting
+ *     for the preceding kernel of the stream, which is safe under ordinary
+ *     stream order.  If the kernel enqueued just before a call lets its
+ *     dependents start early (griddepcontrol.launch_dependents), it must not
+ *     write those inputs after doing so.  The library's own kernels never
+ *     write them; csa2_kv_append and csa2_swa_append, which do, never start
+ *     their dependents early.
  *   - `ws` is a caller-owned device workspace of at least
  *     csa2_workspace_bytes(shape) bytes, 256-byte aligned, zeroed once with
  *     csa2_workspace_init before first use.  Calls that share a workspace
@@ -100,7 +108,8 @@ typedef struct {
   const void* q;       /* [B, H, dk] the layer's own query */
   const void* q_idx;   /* [B, HI, dI] indexer query (Full / Reindex; ignored for Reuse and SWA) */
   const float* w_idx;  /* [B, HI] indexer head weights (Full / Reindex; ignored for Reuse and SWA) */
-  const void* k_swa;   /* [B, W, dk] the layer's own SWA keys, oldest first */
+  const void* k_swa;   /* [B, W, dk] the layer's own SWA keys: rows 0..n_swa-1 in any order
+                          (oldest first, or the ring csa2_swa_append keeps) */
   const void* v_swa;   /* [B, W, dv] the layer's own SWA values */
   float* out;          /* [B, H, dv] attention output */
   float* lse;          /* [B, H] natural-log sum of exp of the scaled logits, or NULL */
@@ -125,6 +134,49 @@ int csa2_workspace_init(void* ws, size_t ws_bytes, csa2_stream_t stream);
  *   kb      [B, ceil(N / block), dI]  (output) */
 int csa2_block_keys(const csa2_shape* shape, const void* k_idx, const int32_t* n_valid,
                     int32_t round_to_int, void* kb, void* ws, size_t ws_bytes, csa2_stream_t stream);
+
+/* Decode-step cache maintenance, main caches (architecture page: the
+ * compressed main KV grows by one entry per compressed span of tokens, and
+ * bullet "Hierarchical indexer" keeps one summary key per block of 8 entries;
+ * producing the compressed entries themselves is a learned operator the pages
+ * do not describe, so they are inputs here).
+ * For each query b, the first n_new[b] rows (0..max_new) of k_new[b],
+ * v_new[b] and kidx_new[b] are written at entry positions n_valid[b],
+ * n_valid[b] + 1, ... of k_main, v_main and k_idx; then, when kb is not NULL,
+ * the summary key of every block those positions fall in is recomputed over
+ * the block's valid entries exactly as csa2_block_keys computes it (other
+ * blocks are left as they are); finally n_valid[b] grows by n_new[b].
+ * Entries that would land at N or beyond are dropped and recorded in the
+ * device error word (bad count).
+ *   k_new [B, max_new, dk]  v_new [B, max_new, dv]  kidx_new [B, max_new, dI]  n_new [B]
+ *   k_main [B, N, dk]  v_main [B, N, dv]  k_idx [B, N, dI]  kb [B, ceil(N / block), dI] or NULL
+ *   n_valid [B] (read and updated)
+ * The caches, kb and n_valid are updated in place; ws holds only the error word. */
+int csa2_kv_append(const csa2_shape* shape, int32_t max_new, const int32_t* n_new, const void* k_new,
+                   const void* v_new, const void* kidx_new, void* k_main, void* v_main, void* k_idx, void* kb,
+                   int32_t* n_valid, int32_t round_to_int, void* ws, size_t ws_bytes, csa2_stream_t stream);
+
+/* One layer's part of csa2_swa_append. */
+typedef struct {
+  const void* k_tok;   /* [B, dk] the layer's key of the new token */
+  const void* v_tok;   /* [B, dv] the layer's value of the new token */
+  void* k_swa;         /* [B, W, dk] the layer's SWA ring (updated in place) */
+  void* v_swa;         /* [B, W, dv] */
+} csa2_swa_slot;
+
+/* Decode-step cache maintenance, SWA windows (architecture page, bullet
+ * "Sparse attention": every query also attends its last W tokens
+ * uncompressed; mode table: every layer has its own SWA KV).
+ * The layers of a group keep their windows as rings that share one head and
+ * one fill count per query: for every layer l and query b, row swa_head[b] of
+ * layers[l].k_swa[b] / v_swa[b] takes layers[l].k_tok[b] / v_tok[b]; then
+ * swa_head[b] advances by one modulo W and n_swa[b] grows by one up to W.
+ * Attention uses rows 0..n_swa[b]-1 as a set, so a ring needs no reordering.
+ * A swa_head or n_swa outside 0..W-1 / 0..W is clamped and recorded in the
+ * device error word (bad count).  1 <= n_layers <= 64; shape.swa >= 1.
+ *   swa_head [B], n_swa [B] (read and updated) */
+int csa2_swa_append(const csa2_shape* shape, const csa2_swa_slot* layers, int32_t n_layers, int32_t* swa_head,
+                    int32_t* n_swa, void* ws, size_t ws_bytes, csa2_stream_t stream);
 
 /* Hierarchical first stage: score every valid block summary key with the
  * indexer formula and keep the top min(P, NB_b) blocks, NB_b = ceil(n_valid[b] / block),

@@ -30,6 +30,11 @@ What it computes, in plain numpy, without blocking, fusion or reordering:
 * attention -- one softmax per query head over the selected main-KV rows
   plus the SWA rows, in float64 on the decoded inputs (page 3 bullet "Sparse
   attention": Top-512 main-KV entries plus a 128-token SWA window).
+* cache maintenance -- appending compressed entries at ``n_valid`` with the
+  summary keys of the touched blocks recomputed, and pushing a decoded token
+  into a ring-shaped SWA window (page 3 bullets "Hierarchical indexer" and
+  "Sparse attention"; the compression operator that makes the entries is
+  not described by the pages, so entries are inputs).
 * layer groups -- Full computes fresh indices, Reindex computes fresh
   indices with its own indexer query over the shared keys, Reuse takes the
   latest indices; every layer has its own query and SWA KV (page 3, "CSA2
@@ -109,6 +114,54 @@ def block_keys(keys: np.ndarray, n_valid: int, block: int, round_to_int: bool,
             mean = round_bf16(mean)
         out[j] = mean
     return out
+
+
+def kv_append(k_main, v_main, k_idx, kb, n_valid, n_new, k_new, v_new, kidx_new, *, block: int,
+              round_to_int: bool, store_bf16: bool = True):
+    """Append ``n_new[b]`` compressed entries per query at position ``n_valid[b]``.
+
+    The cache arrays are copied and returned (rows are moved as stored, so bf16
+    bit patterns stay bit patterns).  Entries that would land past the cache's
+    end are dropped.  When ``kb`` (float64 summary keys, [B, NB, dI]) is given,
+    every block that a new position falls in gets its summary key recomputed
+    from the updated indexer keys with ``block_keys``; other blocks keep their
+    values.  Returns (k_main, v_main, k_idx, kb, n_valid, dropped) where
+    dropped[b] counts the entries that did not fit.
+    """
+    k_main, v_main, k_idx = np.array(k_main), np.array(v_main), np.array(k_idx)
+    kb = None if kb is None else np.array(kb, dtype=np.float64)
+    n_valid = np.array(n_valid, dtype=np.int64)
+    B, N = k_main.shape[0], k_main.shape[1]
+    dropped = np.zeros(B, dtype=np.int64)
+    for b in range(B):
+        nv0 = int(n_valid[b])
+        m = min(int(n_new[b]), N - nv0)
+        dropped[b] = int(n_new[b]) - m
+        k_main[b, nv0:nv0 + m] = k_new[b, :m]
+        v_main[b, nv0:nv0 + m] = v_new[b, :m]
+        k_idx[b, nv0:nv0 + m] = kidx_new[b, :m]
+        nv1 = nv0 + m
+        if kb is not None and m > 0:
+            keys = block_keys(to_f64(k_idx[b]), nv1, block, round_to_int, store_bf16=store_bf16)
+            for j in range(nv0 // block, (nv1 - 1) // block + 1):
+                kb[b, j] = keys[j]
+        n_valid[b] = nv1
+    return k_main, v_main, k_idx, kb, n_valid, dropped
+
+
+def swa_append(k_swa, v_swa, head, n_swa, k_tok, v_tok):
+    """Push token b into query b's SWA ring: row ``head[b]`` takes it, ``head``
+    advances modulo the window, ``n_swa`` grows up to the window.  Returns
+    updated copies (k_swa, v_swa, head, n_swa)."""
+    k_swa, v_swa = np.array(k_swa), np.array(v_swa)
+    head, n_swa = np.array(head, dtype=np.int64), np.array(n_swa, dtype=np.int64)
+    W = k_swa.shape[1]
+    for b in range(k_swa.shape[0]):
+        k_swa[b, head[b]] = k_tok[b]
+        v_swa[b, head[b]] = v_tok[b]
+        head[b] = (head[b] + 1) % W
+        n_swa[b] = min(n_swa[b] + 1, W)
+    return k_swa, v_swa, head, n_swa
 
 
 # ----------------------------------------------------------------------------

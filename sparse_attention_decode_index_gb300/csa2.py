@@ -52,6 +52,9 @@ _SIGS = {
     "csa2_workspace_bytes": (_SZ, [ctypes.POINTER(CShape)]),
     "csa2_workspace_init": (ctypes.c_int, [_VP, _SZ, _VP]),
     "csa2_block_keys": (ctypes.c_int, [ctypes.POINTER(CShape), _VP, _VP, _I32, _VP, _VP, _SZ, _VP]),
+    "csa2_kv_append": (ctypes.c_int, [ctypes.POINTER(CShape), _I32, _VP, _VP, _VP, _VP, _VP, _VP, _VP, _VP, _VP,
+                                      _I32, _VP, _SZ, _VP]),
+    "csa2_swa_append": (ctypes.c_int, [ctypes.POINTER(CShape), ctypes.c_void_p, _I32, _VP, _VP, _VP, _SZ, _VP]),
     "csa2_index_blocks": (ctypes.c_int, [ctypes.POINTER(CShape), _VP, _VP, _VP, _VP, _VP, _VP, _VP, _SZ, _VP]),
     "csa2_index_tokens": (ctypes.c_int, [ctypes.POINTER(CShape), _VP, _VP, _VP, _VP, _VP, _VP, _VP, _VP, _VP,
                                          _VP, _SZ, _VP]),
@@ -167,6 +170,38 @@ def block_keys(shape, k_idx, n_valid, kb, ws, round_to_int: bool = True, stream=
     _check(lib().csa2_block_keys(ctypes.byref(s), _ptr(k_idx, e, "k_idx"), _ptr(n_valid, torch.int32, "n_valid"),
                                  int(bool(round_to_int)), _ptr(kb, e, "kb"), _ptr(ws, torch.uint8, "ws"),
                                  ws.numel(), _stream(stream)), "csa2_block_keys")
+
+
+def kv_append(shape, n_new, k_new, v_new, kidx_new, k_main, v_main, k_idx, kb, n_valid, ws,
+              round_to_int: bool = True, stream=None):
+    """Append n_new[b] compressed entries per query (rows of k_new / v_new / kidx_new, shaped
+    [B, max_new, ...]) at n_valid[b]; recompute the touched block keys (kb may be None); grow n_valid."""
+    s = c_shape(shape)
+    e = elem_dtype(shape)
+    max_new = int(k_new.shape[1]) if k_new is not None else 0
+    _check(lib().csa2_kv_append(ctypes.byref(s), max_new, _ptr(n_new, torch.int32, "n_new"), _ptr(k_new, e, "k_new"),
+                                _ptr(v_new, e, "v_new"), _ptr(kidx_new, e, "kidx_new"), _ptr(k_main, e, "k_main"),
+                                _ptr(v_main, e, "v_main"), _ptr(k_idx, e, "k_idx"), _ptr(kb, e, "kb"),
+                                _ptr(n_valid, torch.int32, "n_valid"), int(bool(round_to_int)),
+                                _ptr(ws, torch.uint8, "ws"), ws.numel(), _stream(stream)), "csa2_kv_append")
+
+
+class CSwaSlot(ctypes.Structure):
+    _fields_ = [("k_tok", ctypes.c_void_p), ("v_tok", ctypes.c_void_p), ("k_swa", ctypes.c_void_p),
+                ("v_swa", ctypes.c_void_p)]
+
+
+def swa_append(shape, slots, swa_head, n_swa, ws, stream=None):
+    """Push one token per query into the SWA ring of every layer in ``slots`` (a list of
+    (k_tok [B, dk], v_tok [B, dv], k_swa [B, W, dk], v_swa [B, W, dv])); the shared
+    swa_head advances once and n_swa grows up to W."""
+    s = c_shape(shape)
+    e = elem_dtype(shape)
+    arr = (CSwaSlot * len(slots))(*[CSwaSlot(_ptr(kt, e, "k_tok"), _ptr(vt, e, "v_tok"), _ptr(ks, e, "k_swa"),
+                                             _ptr(vs, e, "v_swa")) for kt, vt, ks, vs in slots])
+    _check(lib().csa2_swa_append(ctypes.byref(s), ctypes.cast(arr, ctypes.c_void_p), len(slots),
+                                 _ptr(swa_head, torch.int32, "swa_head"), _ptr(n_swa, torch.int32, "n_swa"),
+                                 _ptr(ws, torch.uint8, "ws"), ws.numel(), _stream(stream)), "csa2_swa_append")
 
 
 def index_blocks(shape, q_idx, w, kb, n_valid, pool_out, n_pool_out, ws, stream=None):

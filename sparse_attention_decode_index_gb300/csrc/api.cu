@@ -335,6 +335,67 @@ int csa2_block_keys(const csa2_shape* shape, const void* k_idx, const int32_t* n
   return cuda_status(launch_block_keys(a, s.batch, stream));
 }
 
+int csa2_kv_append(const csa2_shape* shape, int32_t max_new, const int32_t* n_new, const void* k_new,
+                   const void* v_new, const void* kidx_new, void* k_main, void* v_main, void* k_idx, void* kb,
+                   int32_t* n_valid, int32_t round_to_int, void* ws, size_t ws_bytes, csa2_stream_t stream) {
+  CSA2_TRY(check_shape(shape));
+  const csa2_shape& s = *shape;
+  CSA2_TRY(check_ws(s, ws, ws_bytes));
+  if (max_new < 0 || max_new > s.n_entries) return CSA2_ERR_INVALID_ARG;
+  if (n_new == nullptr || n_valid == nullptr || k_main == nullptr || v_main == nullptr || k_idx == nullptr)
+    return CSA2_ERR_INVALID_ARG;
+  if (max_new > 0 && (k_new == nullptr || v_new == nullptr || kidx_new == nullptr)) return CSA2_ERR_INVALID_ARG;
+  if (round_to_int != 0 && round_to_int != 1) return CSA2_ERR_INVALID_ARG;
+  const WsLayout L = layout(s);
+  KvAppendArgs a{};
+  a.n_new = n_new;
+  a.max_new = max_new;
+  a.k_new = k_new;
+  a.v_new = v_new;
+  a.kidx_new = kidx_new;
+  a.k_main = k_main;
+  a.v_main = v_main;
+  a.k_idx = k_idx;
+  a.kb = kb;
+  a.n_valid = n_valid;
+  a.n_entries = s.n_entries;
+  a.nb_cap = int(L.nb_cap);
+  a.k_dim = s.k_dim;
+  a.v_dim = s.v_dim;
+  a.idx_dim = s.idx_dim;
+  a.block = s.block;
+  a.round_to_int = round_to_int;
+  a.dtype = s.dtype;
+  a.err = at<int>(ws, L.hdr);
+  return cuda_status(launch_kv_append(a, s.batch, stream));
+}
+
+int csa2_swa_append(const csa2_shape* shape, const csa2_swa_slot* layers, int32_t n_layers, int32_t* swa_head,
+                    int32_t* n_swa, void* ws, size_t ws_bytes, csa2_stream_t stream) {
+  CSA2_TRY(check_shape(shape));
+  const csa2_shape& s = *shape;
+  CSA2_TRY(check_ws(s, ws, ws_bytes));
+  if (s.swa < 1 || layers == nullptr || n_layers < 1 || n_layers > kMaxSwaLayers) return CSA2_ERR_INVALID_ARG;
+  if (swa_head == nullptr || n_swa == nullptr) return CSA2_ERR_INVALID_ARG;
+  const WsLayout L = layout(s);
+  SwaAppendArgs a{};
+  for (int l = 0; l < n_layers; ++l) {
+    const csa2_swa_slot& y = layers[l];
+    if (y.k_tok == nullptr || y.v_tok == nullptr || y.k_swa == nullptr || y.v_swa == nullptr)
+      return CSA2_ERR_INVALID_ARG;
+    a.slot[l] = SwaAppendArgs::Slot{y.k_tok, y.v_tok, y.k_swa, y.v_swa};
+  }
+  a.n_layers = n_layers;
+  a.head = swa_head;
+  a.n_swa = n_swa;
+  a.swa = s.swa;
+  a.k_dim = s.k_dim;
+  a.v_dim = s.v_dim;
+  a.dtype = s.dtype;
+  a.err = at<int>(ws, L.hdr);
+  return cuda_status(launch_swa_append(a, s.batch, stream));
+}
+
 int csa2_index_blocks(const csa2_shape* shape, const void* q_idx, const float* w, const void* kb,
                       const int32_t* n_valid, int32_t* pool_out, int32_t* n_pool_out, void* ws, size_t ws_bytes,
                       csa2_stream_t stream) {

@@ -217,4 +217,21 @@ CSA2_DEV void store_elem(void* base, long long i, int dtype, float v) {
     static_cast<__nv_bfloat16*>(base)[i] = __float2bfloat16_rn(v);
 }
 
+// Block summary key element (b, block j, dim d): the mean of k_idx over the
+// block's valid entries (j*block .. min((j+1)*block, nv) - 1), summed in entry
+// order in fp32, optionally rounded half-to-even; 0 for a block with no valid
+// entry.  Shared by the from-scratch and the incremental (append) kernels so
+// that both give bit-identical keys.
+CSA2_DEV float block_key_elem(const void* k_idx, long long row0, int dim, int block, int nv, int j, int d,
+                              int dtype, int round_to_int) {
+  const int r0 = j * block;
+  const int c = min(block, nv - r0);
+  if (c <= 0) return 0.f;
+  float s = 0.f;
+  for (int r = 0; r < c; ++r) s += load_elem(k_idx, (row0 + r0 + r) * dim + d, dtype);
+  float v = s / float(c);
+  if (round_to_int) v = rintf(v);
+  return v;
+}
+
 }  // namespace csa2

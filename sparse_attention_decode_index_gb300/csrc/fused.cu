@@ -151,7 +151,6 @@ __global__ void __launch_bounds__(kThreads, 4) index_select_kernel(const SelectA
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const uint32_t crank = cluster_rank(), ncta = cluster_size();
 
-  const int nv = clamp_count(a.n_valid[b], a.valid_cap, a.err);
   if (tid == 0) {
     for (int s = 0; s < kStages; ++s) {
       mbar_init(&sm.full[s], 1);
@@ -160,6 +159,7 @@ __global__ void __launch_bounds__(kThreads, 4) index_select_kernel(const SelectA
     mbar_fence_init();
   }
   pdl_wait();   // the pool / n_pool come from the preceding launch
+  const int nv = clamp_count(a.n_valid[b], a.valid_cap, a.err);
 
   // ---------------- this CTA's share of the query's candidates
   int n_units;

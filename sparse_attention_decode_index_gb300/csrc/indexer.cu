@@ -274,15 +274,8 @@ __global__ void __launch_bounds__(256) block_keys_kernel(const BlockKeyArgs a) {
   if (i >= (long long)a.nb_cap * a.dim) return;
   const int j = int(i / a.dim), d = int(i % a.dim);
   const int nv = clamp_count(a.n_valid[b], a.n_entries, a.err);
-  const int r0 = j * a.block;
-  const int c = min(a.block, nv - r0);
-  float v = 0.f;
-  if (c > 0) {
-    float s = 0.f;
-    for (int r = 0; r < c; ++r) s += load_elem(a.k_idx, ((long long)b * a.n_entries + r0 + r) * a.dim + d, a.dtype);
-    v = s / float(c);
-    if (a.round_to_int) v = rintf(v);
-  }
+  const float v = block_key_elem(a.k_idx, (long long)b * a.n_entries, a.dim, a.block, nv, j, d, a.dtype,
+                                 a.round_to_int);
   store_elem(a.kb, ((long long)b * a.nb_cap + j) * a.dim + d, a.dtype, v);
 }
 

@@ -101,6 +101,41 @@ struct BlockKeyArgs {
   int* err;
 };
 
+// Decode-step cache maintenance (append.cu).
+struct KvAppendArgs {
+  const int* n_new;          // [B]
+  int max_new;
+  const void* k_new;         // [B, max_new, k_dim]
+  const void* v_new;         // [B, max_new, v_dim]
+  const void* kidx_new;      // [B, max_new, idx_dim]
+  void* k_main;              // [B, N, k_dim]
+  void* v_main;              // [B, N, v_dim]
+  void* k_idx;               // [B, N, idx_dim]
+  void* kb;                  // [B, nb_cap, idx_dim] or null
+  int* n_valid;              // [B] (read and updated)
+  int n_entries, nb_cap, k_dim, v_dim, idx_dim, block, round_to_int, dtype;
+  int* err;
+};
+
+constexpr int kMaxSwaLayers = 64;
+
+struct SwaAppendArgs {
+  struct Slot {
+    const void* k_tok;       // [B, k_dim]
+    const void* v_tok;       // [B, v_dim]
+    void* k_swa;             // [B, W, k_dim]
+    void* v_swa;             // [B, W, v_dim]
+  } slot[kMaxSwaLayers];
+  int n_layers;
+  int* head;                 // [B] (read and updated)
+  int* n_swa;                // [B] (read and updated)
+  int swa, k_dim, v_dim, dtype;
+  int* err;
+};
+
+cudaError_t launch_kv_append(const KvAppendArgs& a, int batch, cudaStream_t st);
+cudaError_t launch_swa_append(const SwaAppendArgs& a, int batch, cudaStream_t st);
+
 int device_sm_count();
 
 // Launch `kernel` with programmatic stream serialization (PDL) and an optional

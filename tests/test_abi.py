@@ -34,7 +34,8 @@ def declared_functions():
 def test_header_declares_the_planned_entry_points():
     names = declared_functions()
     for n in ("csa2_index_blocks", "csa2_index_tokens", "csa2_topk", "csa2_sparse_attn", "csa2_layer_group",
-              "csa2_block_keys", "csa2_workspace_bytes", "csa2_status_str", "csa2_read_device_error"):
+              "csa2_block_keys", "csa2_workspace_bytes", "csa2_status_str", "csa2_read_device_error",
+              "csa2_kv_append", "csa2_swa_append"):
         assert n in names
 
 
@@ -103,6 +104,42 @@ def test_entry_points_reject_bad_arguments_before_launch(csa2):
     # Top-k larger than a chunk, and merges that would not shrink the list
     assert lib.csa2_topk(ctypes.byref(s), FAKE, 100, None, None, 20000, FAKE, None, FAKE, wsb, None) == UNSUPPORTED
     assert lib.csa2_topk(ctypes.byref(s), FAKE, 40000, None, None, 9000, FAKE, None, FAKE, wsb, None) == UNSUPPORTED
+
+
+def test_append_entry_points_reject_bad_arguments_before_launch(csa2):
+    lib = csa2.lib()
+    s = csa2.c_shape(_shape())
+    wsb = lib.csa2_workspace_bytes(ctypes.byref(s))
+    ok_args = [FAKE] * 9          # n_new, k_new, v_new, kidx_new, k_main, v_main, k_idx, kb, n_valid
+
+    def kv(max_new=1, args=None, rnd=1, ws=FAKE, bytes_=wsb):
+        a = ok_args if args is None else args
+        return lib.csa2_kv_append(ctypes.byref(s), max_new, *a, rnd, ws, bytes_, None)
+
+    assert kv(max_new=-1) == INVALID                         # negative row count
+    assert kv(max_new=10 ** 9) == INVALID                    # more rows than the cache holds
+    assert kv(args=[None] + ok_args[1:]) == INVALID           # n_new missing
+    assert kv(args=ok_args[:1] + [None] + ok_args[2:]) == INVALID   # k_new missing while max_new > 0
+    assert kv(args=ok_args[:8] + [None]) == INVALID           # n_valid missing
+    assert kv(rnd=2) == INVALID
+    assert kv(bytes_=wsb - 1) == WORKSPACE
+    assert kv(ws=FAKE + 16) == WORKSPACE                      # misaligned workspace
+    slot = csa2.CSwaSlot(FAKE, FAKE, FAKE, FAKE)
+    slots = (csa2.CSwaSlot * 2)(slot, slot)
+    sp = ctypes.cast(slots, ctypes.c_void_p)
+
+    def swa(shape_, sl=sp, n=2, head=FAKE, n_swa=FAKE, bytes_=None):
+        b_ = lib.csa2_workspace_bytes(ctypes.byref(shape_)) if bytes_ is None else bytes_
+        return lib.csa2_swa_append(ctypes.byref(shape_), sl, n, head, n_swa, FAKE, b_, None)
+
+    assert swa(csa2.c_shape(_shape(swa=0))) == INVALID       # no window
+    assert swa(s, n=0) == INVALID
+    assert swa(s, n=65) == INVALID                            # more layers than one call takes
+    assert swa(s, sl=None) == INVALID
+    assert swa(s, head=None) == INVALID
+    assert swa(s, bytes_=wsb - 1) == WORKSPACE
+    bad = (csa2.CSwaSlot * 2)(slot, csa2.CSwaSlot(FAKE, None, FAKE, FAKE))
+    assert swa(s, sl=ctypes.cast(bad, ctypes.c_void_p)) == INVALID
 
 
 def _layers(csa2, modes, hier=None):

@@ -16,7 +16,10 @@ PINS = [P.test_golden_toy16_hand, P.test_indexer_scores_match_integer_loops,
         P.test_hierarchical_equals_flat_when_pool_covers_every_block,
         P.test_reuse_layers_return_the_indexing_layers_indices,
         P.test_attention_closed_forms, P.test_toy16_structure,
-        lambda: P.test_sparse_equals_dense_causal_attention_naive(24, 8, 16)]
+        lambda: P.test_sparse_equals_dense_causal_attention_naive(24, 8, 16),
+        P.test_kv_append_in_steps_equals_the_cache_written_at_once,
+        P.test_kv_append_touches_only_the_blocks_of_the_new_positions,
+        P.test_swa_ring_holds_the_last_w_tokens]
 
 
 def _topk_highest_id_wins(scores, ids, k):
@@ -68,6 +71,33 @@ def _pool_unsorted(q_idx, w, kb, n_blocks, pool, relu=True):
 
 
 _orig_attend = C.attend
+_orig_kv_append = C.kv_append
+_orig_swa_append = C.swa_append
+
+
+def _kv_append_one_slot_late(k_main, v_main, k_idx, kb, n_valid, *rest, **kw):
+    return _orig_kv_append(k_main, v_main, k_idx, kb, np.asarray(n_valid) + 1, *rest, **kw)
+
+
+def _kv_append_stale_last_block(k_main, v_main, k_idx, kb, n_valid, n_new, k_new, v_new, kidx_new, *, block,
+                                round_to_int, store_bf16=True):
+    # recomputes only the blocks that were already valid before the append
+    k1, v1, x1, kb1, nv1, dr = _orig_kv_append(k_main, v_main, k_idx, None, n_valid, n_new, k_new, v_new, kidx_new,
+                                               block=block, round_to_int=round_to_int, store_bf16=store_bf16)
+    if kb is not None:
+        kb1 = np.array(kb, dtype=np.float64)
+        for b in range(len(nv1)):
+            nv0 = int(n_valid[b])
+            keys = C.block_keys(C.to_f64(x1[b]), int(nv1[b]), block, round_to_int, store_bf16=store_bf16)
+            for j in range(nv0 // block, -(-nv0 // block)):
+                kb1[b, j] = keys[j]
+    return k1, v1, x1, kb1, nv1, dr
+
+
+def _swa_append_head_stuck(k_swa, v_swa, head, n_swa, k_tok, v_tok):
+    k1, v1, _, n1 = _orig_swa_append(k_swa, v_swa, head, n_swa, k_tok, v_tok)
+    return k1, v1, np.array(head), n1
+
 
 MUTATIONS = {
     "tie-break keeps the highest id": ("select_topk", _topk_highest_id_wins),
@@ -78,6 +108,9 @@ MUTATIONS = {
     "softmax scale dropped": ("attend", _attend_without_scale),
     "pooled entries shifted by one": ("pooled_entries", _pooled_entries_off_by_one),
     "pool left in score order": ("pool_blocks", _pool_unsorted),
+    "appended entries land one slot late": ("kv_append", _kv_append_one_slot_late),
+    "summary key of a newly opened block not computed": ("kv_append", _kv_append_stale_last_block),
+    "SWA ring head never advances": ("swa_append", _swa_append_head_stuck),
 }
 
 

@@ -305,3 +305,103 @@ def test_swa_layer_is_window_only_attention():
             assert np.allclose(res[li]["out"][b], ref_out, atol=1e-12)
             assert np.allclose(res[li]["lse"][b], ref_lse, atol=1e-12)
     assert "idx" not in res[0]
+
+
+# ---------------------------------------------------------------- cache maintenance (append)
+
+def _bf16_ints(rng, shape):
+    return W.f32_to_bf16_bits(rng.integers(-4, 5, shape).astype(np.float32))
+
+
+def test_kv_append_in_steps_equals_the_cache_written_at_once():
+    """Entries appended in random-sized steps, some past the cache's end, give the
+    cache written in one go: the rows in arrival order, n_valid capped at N, and
+    summary keys equal to block_keys over the final cache (blocks past the
+    valid entries untouched)."""
+    rng = np.random.default_rng(5)
+    B, N, dk, dv, dI, blk = 3, 37, 3, 2, 4, 8
+    start = np.array([0, 11, 30])
+    k_main = rng.integers(0, 60000, (B, N, dk)).astype(np.uint16)     # rows past n_valid: arbitrary
+    v_main = rng.integers(0, 60000, (B, N, dv)).astype(np.uint16)
+    k_idx = _bf16_ints(rng, (B, N, dI))
+    nb = -(-N // blk)
+    kb = np.zeros((B, nb, dI))
+    for b in range(B):
+        nbv = -(-int(start[b]) // blk)
+        kb[b, :nbv] = oracle.block_keys(oracle.to_f64(k_idx[b]), int(start[b]), blk, True)
+    T = 40                                                              # more than fits for every query
+    ks = rng.integers(0, 60000, (B, T, dk)).astype(np.uint16)
+    vs = rng.integers(0, 60000, (B, T, dv)).astype(np.uint16)
+    xs = _bf16_ints(rng, (B, T, dI))
+    cur = (k_main, v_main, k_idx, kb, start.copy())
+    fed = np.zeros(B, dtype=np.int64)
+    dropped = np.zeros(B, dtype=np.int64)
+    while (fed < T).any():
+        n_new = np.minimum(rng.integers(0, 5, B), T - fed)
+        mx = int(n_new.max()) if n_new.max() > 0 else 1
+        take = lambda a, d: np.stack([np.pad(a[b, fed[b]:fed[b] + n_new[b]], ((0, mx - n_new[b]), (0, 0)))
+                                      for b in range(B)])
+        *cur, dr = oracle.kv_append(*cur, n_new, take(ks, dk), take(vs, dv), take(xs, dI), block=blk,
+                                    round_to_int=True)
+        fed += n_new
+        dropped += dr
+    k1, v1, x1, kb1, nv1 = cur
+    for b in range(B):
+        fit = N - start[b]
+        assert nv1[b] == N and dropped[b] == T - fit
+        assert np.array_equal(k1[b, :start[b]], k_main[b, :start[b]])
+        assert np.array_equal(k1[b, start[b]:], ks[b, :fit])
+        assert np.array_equal(v1[b, start[b]:], vs[b, :fit])
+        assert np.array_equal(x1[b, start[b]:], xs[b, :fit])
+        full = oracle.block_keys(oracle.to_f64(x1[b]), N, blk, True)
+        assert np.array_equal(kb1[b], full)
+
+
+def test_kv_append_touches_only_the_blocks_of_the_new_positions():
+    keys = np.arange(40, dtype=np.float64).reshape(20, 2)        # entry e has keys (2e, 2e+1)
+    k_idx = np.zeros((1, 24, 2))
+    k_idx[0, :20] = keys
+    kb = np.full((1, 3, 2), 99.0)                                # stale values everywhere
+    new = np.array([[[100.0, 101.0], [102.0, 103.0]]])
+    _, _, x, kb1, nv, dr = oracle.kv_append(np.zeros((1, 24, 1)), np.zeros((1, 24, 1)), k_idx, kb, [15], [2],
+                                            np.zeros((1, 2, 1)), np.zeros((1, 2, 1)), new, block=8,
+                                            round_to_int=False, store_bf16=False)
+    assert nv.tolist() == [17] and dr.tolist() == [0]
+    assert x[0, 15].tolist() == [100.0, 101.0] and x[0, 16].tolist() == [102.0, 103.0]
+    # block 1 holds entries 8..15: keys 16..29 (even) / 17..31 (odd) with entry 15 replaced by (100, 101)
+    assert kb1[0, 1].tolist() == [(sum(range(16, 30, 2)) + 100) / 8, (sum(range(17, 31, 2)) + 101) / 8]
+    assert kb1[0, 2].tolist() == [102.0, 103.0]                 # block 2 holds entry 16 only
+    assert kb1[0, 0].tolist() == [99.0, 99.0]                   # block 0 untouched
+
+
+def test_swa_ring_holds_the_last_w_tokens():
+    from collections import deque
+    Wn, T, B = 5, 13, 2
+    rng = np.random.default_rng(9)
+    toks = rng.integers(0, 60000, (T, B, 3)).astype(np.uint16)
+    k_swa = np.zeros((B, Wn, 3), dtype=np.uint16)
+    v_swa = np.zeros((B, Wn, 3), dtype=np.uint16)
+    head, n = np.zeros(B, dtype=np.int64), np.zeros(B, dtype=np.int64)
+    last = [deque(maxlen=Wn) for _ in range(B)]
+    for t in range(T):
+        k_swa, v_swa, head, n = oracle.swa_append(k_swa, v_swa, head, n, toks[t], toks[t] + 1)
+        for b in range(B):
+            last[b].append(tuple(toks[t, b]))
+            assert n[b] == min(t + 1, Wn) and head[b] == (t + 1) % Wn
+            assert sorted(tuple(r) for r in k_swa[b, :n[b]]) == sorted(last[b])
+            assert sorted(tuple(r) for r in v_swa[b, :n[b]]) == sorted(tuple(np.array(x) + 1) for x in last[b])
+
+
+def test_attention_over_the_ring_equals_attention_oldest_first():
+    rng = np.random.default_rng(3)
+    H, dk, dv, Wn, N = 4, 6, 5, 7, 20
+    q = rng.standard_normal((H, dk))
+    k_main, v_main = rng.standard_normal((N, dk)), rng.standard_normal((N, dv))
+    idx = np.array([3, 8, 11, -1])
+    k_old, v_old = rng.standard_normal((Wn, dk)), rng.standard_normal((Wn, dv))
+    shift = 4                                                    # ring after Wn + 4 appends
+    ring = np.roll(np.arange(Wn), shift)
+    a = oracle.sparse_attention(q, k_main, v_main, idx, k_old, v_old, Wn, 0.4)
+    b = oracle.sparse_attention(q, k_main, v_main, idx, k_old[ring], v_old[ring], Wn, 0.4)
+    np.testing.assert_allclose(a[0], b[0], rtol=0, atol=1e-12)
+    np.testing.assert_allclose(a[1], b[1], rtol=0, atol=1e-12)
