@@ -21,6 +21,7 @@ cores.
 from __future__ import annotations
 
 import argparse
+import dataclasses
 import json
 import math
 import multiprocessing as mp
@@ -394,6 +395,7 @@ def run_ours(args):
     roof = dominant_kernel_roofline(csa2, wl, d, stream, flush, args, peak, peak_src)
     step_gbs = ab["total"] / (ms_per_step / 1e3) / 1e9
     e2e = end_to_end(csa2, wl, d, graph, stream, flush, args, dev)
+    append = append_timing(csa2, wl, stream, args)
     clocks = clk.summary()
     clocks["window"] = (f"nvidia-smi every 200 ms over the timed steps plus {args.clock_soak:.1f} s before and "
                         f"{args.clock_soak / 2:.1f} s after of untimed replays of the same step")
@@ -419,7 +421,8 @@ def run_ours(args):
                                   "frac": step_gbs / peak, "alg_bytes_per_step": ab["total"],
                                   "alg_bytes_breakdown": ab, "peak_source": peak_src,
                                   "frac_of_nominal_8TBs": step_gbs / 8000.0},
-                "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": per_step_launches * args.steps,
+                "cpu_baseline": cpu, "e2e": e2e, "append": append,
+                "gpu_launches": per_step_launches * args.steps,
                 "launches_per_step": per_step_launches, "clocks": clocks,
                 "step_ms": {"median": statistics.median(step_ms), "min": min(step_ms), "max": max(step_ms)}}
         print(json.dumps(line))
@@ -500,6 +503,76 @@ def dominant_kernel_roofline(csa2, wl, d, stream, flush, args, peak, peak_src):
             "traffic": traffic, "traffic_source": traffic_src, "alg_bytes_per_launch": alg, "launch_us": 1e3 * avg,
             "peak_source": peak_src,
             "timing": f"alone, {reps} launches, CUDA events on its stream, L2 flushed before each"}
+
+
+def append_timing(csa2, wl, stream, args):
+    """Decode-step cache maintenance at the workload's batch and dims: one new compressed
+    entry per query (csa2_kv_append, block keys kept) and one token per query into one
+    layer's SWA ring (csa2_swa_append), each timed alone on its stream: device time per call
+    from CUDA graphs of back-to-back calls.
+    Runs on buffers of its own (1,024-entry caches; the cost does not depend on the
+    cache length), after every other measurement."""
+    import torch
+    sh = dataclasses.replace(wl.shape, n_entries=1024, tokens=1)   # appends are per sequence
+    B, dev = sh.batch, torch.device("cuda")
+    bf = torch.bfloat16
+    k_main = torch.zeros((B, sh.n_entries, sh.k_dim), dtype=bf, device=dev)
+    v_main = torch.zeros((B, sh.n_entries, sh.v_dim), dtype=bf, device=dev)
+    k_idx = torch.zeros((B, sh.n_entries, sh.idx_dim), dtype=bf, device=dev)
+    kb = torch.zeros((B, sh.n_entries // sh.block, sh.idx_dim), dtype=bf, device=dev)
+    k_new = torch.ones((B, 1, sh.k_dim), dtype=bf, device=dev)
+    v_new = torch.ones((B, 1, sh.v_dim), dtype=bf, device=dev)
+    x_new = torch.ones((B, 1, sh.idx_dim), dtype=bf, device=dev)
+    n_new = torch.ones(B, dtype=torch.int32, device=dev)
+    n_valid = torch.zeros(B, dtype=torch.int32, device=dev)
+    k_swa = torch.zeros((B, sh.swa, sh.k_dim), dtype=bf, device=dev)
+    v_swa = torch.zeros((B, sh.swa, sh.v_dim), dtype=bf, device=dev)
+    k_tok = torch.ones((B, sh.k_dim), dtype=bf, device=dev)
+    v_tok = torch.ones((B, sh.v_dim), dtype=bf, device=dev)
+    head = torch.zeros(B, dtype=torch.int32, device=dev)
+    n_swa = torch.zeros(B, dtype=torch.int32, device=dev)
+    ws = csa2.workspace(sh)
+    reps = max(args.steps, 20)
+
+    per = 16                                                     # calls per captured graph
+
+    def timed(fn, reset):
+        """Median device time per call: graphs of `per` back-to-back calls replayed with
+        CUDA events around each replay (so host-side argument marshalling is not timed)."""
+        with torch.cuda.stream(stream):
+            reset()
+            fn()                                                 # warm-up outside capture
+            reset()
+        torch.cuda.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            for _ in range(per):
+                fn()
+        evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(reps)]
+        with torch.cuda.stream(stream):
+            for i in range(3):
+                reset()
+                g.replay()
+            for e0, e1 in evs:
+                reset()
+                e0.record(stream)
+                g.replay()
+                e1.record(stream)
+        torch.cuda.synchronize()
+        return statistics.median(e0.elapsed_time(e1) for e0, e1 in evs) * 1e3 / per
+
+    us_kv = timed(lambda: csa2.kv_append(sh, n_new, k_new, v_new, x_new, k_main, v_main, k_idx, kb, n_valid, ws,
+                                         stream=stream), lambda: n_valid.zero_())
+    us_swa = timed(lambda: csa2.swa_append(sh, [(k_tok, v_tok, k_swa, v_swa)], head, n_swa, ws, stream=stream),
+                   lambda: (head.zero_(), n_swa.zero_()))
+    st, bits = csa2.read_device_error(ws, stream)
+    row = 2 * (sh.k_dim + sh.v_dim + sh.idx_dim)                 # one entry read and written
+    kv_bytes = B * (row + sh.block * 2 * sh.idx_dim + 2 * sh.idx_dim)   # + block rows read, summary written
+    swa_bytes = B * 2 * 2 * (sh.k_dim + sh.v_dim)
+    return {"workload": f"batch {B}, one new compressed entry and one SWA token per query",
+            "kv_append_us": us_kv, "kv_append_bytes": kv_bytes, "swa_append_us": us_swa,
+            "swa_append_bytes": swa_bytes, "bound": "launch latency (one CTA per query, KBs per call)",
+            "device_error_bits": bits}
 
 
 def end_to_end(csa2, wl, d, graph, stream, flush, args, dev):

@@ -99,6 +99,14 @@ typedef struct {
   float scale;         /* softmax scale; <= 0 selects 1/sqrt(dk) */
   int32_t relu;        /* 1: ReLU on each indexer head's dot product (default reading); 0: none */
   int32_t dtype;       /* csa2_dtype */
+  int32_t tokens;      /* T: query tokens per sequence (0 or 1: one).  With T > 1 (architecture
+                          page, "Asymmetric encoder-decoder": prompt tokens run a 128-token decoder
+                          replay), B is a multiple of T and queries b = s*T .. s*T + T-1 share the
+                          caches of sequence s: k_main, v_main and k_idx are then [B / T, N, ...].
+                          Everything else stays per query, including n_valid (each token's own
+                          causal count), the SWA rows and kb (block summary keys of the query's own
+                          valid prefix, so a token's partial last block averages only entries it
+                          may see).  csa2_kv_append and csa2_swa_append take T <= 1. */
 } csa2_shape;
 
 /* One layer of a group (csa2_layer_group). */

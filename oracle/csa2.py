@@ -261,8 +261,11 @@ def run_group(wl, *, queries: Optional[List[int]] = None, want_attention: bool =
     [B', H, dv] and ``lse`` [B', H] (if ``want_attention``), and for indexing
     layers the per-query intermediates (``pool``, ``cand``, ``scores``).
     ``queries`` restricts the run to a subset of the batch (sampled parity).
+    With ``shape.tokens`` = T > 1 the caches hold one sequence per T queries
+    and query b reads sequence b // T; every other array is per query.
     """
     sh = wl.shape
+    tokens = max(1, int(getattr(sh, "tokens", 1)))
     relu = bool(sh.relu) if relu is None else relu
     scale = sh.scale if sh.scale > 0 else 1.0 / math.sqrt(sh.k_dim)
     qs = list(range(sh.batch)) if queries is None else list(queries)
@@ -271,12 +274,13 @@ def run_group(wl, *, queries: Optional[List[int]] = None, want_attention: bool =
     for bi, b in enumerate(qs):
         n_valid = int(wl.n_valid[b])
         n_swa = int(wl.n_swa[b])
-        keys = to_f64(wl.k_idx[b])
+        seq = b // tokens
+        keys = to_f64(wl.k_idx[seq])
         kb = None
         if any(L.hier for L in wl.layers):
             kb = block_keys(keys, n_valid, sh.block, bool(wl.round_block_keys), store_bf16=bf16)
-        k_main = to_f64(wl.k_main[b]) if want_attention else None
-        v_main = to_f64(wl.v_main[b]) if want_attention else None
+        k_main = to_f64(wl.k_main[seq]) if want_attention else None
+        v_main = to_f64(wl.v_main[seq]) if want_attention else None
         cur = None
         for li, L in enumerate(wl.layers):
             r = results[li]

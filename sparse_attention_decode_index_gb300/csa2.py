@@ -36,7 +36,7 @@ class CShape(ctypes.Structure):
                 ("idx_dim", ctypes.c_int32), ("block", ctypes.c_int32), ("pool_blocks", ctypes.c_int32),
                 ("topk", ctypes.c_int32), ("q_heads", ctypes.c_int32), ("k_dim", ctypes.c_int32),
                 ("v_dim", ctypes.c_int32), ("swa", ctypes.c_int32), ("scale", ctypes.c_float),
-                ("relu", ctypes.c_int32), ("dtype", ctypes.c_int32)]
+                ("relu", ctypes.c_int32), ("dtype", ctypes.c_int32), ("tokens", ctypes.c_int32)]
 
 
 class CLayer(ctypes.Structure):
@@ -110,7 +110,7 @@ def c_shape(shape) -> CShape:
     return CShape(int(shape.batch), int(shape.n_entries), int(shape.idx_heads), int(shape.idx_dim),
                   int(shape.block), int(shape.pool_blocks), int(shape.topk), int(shape.q_heads),
                   int(shape.k_dim), int(shape.v_dim), int(shape.swa), float(getattr(shape, "scale", 0.0)),
-                  int(getattr(shape, "relu", 1)), int(dt))
+                  int(getattr(shape, "relu", 1)), int(dt), int(getattr(shape, "tokens", 1)))
 
 
 def elem_dtype(shape) -> torch.dtype:

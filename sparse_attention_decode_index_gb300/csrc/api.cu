@@ -89,6 +89,7 @@ int check_shape(const csa2_shape* s) {
     return CSA2_ERR_INVALID_ARG;
   if (s->dtype != CSA2_BF16 && s->dtype != CSA2_F32) return CSA2_ERR_INVALID_ARG;
   if (s->relu != 0 && s->relu != 1) return CSA2_ERR_INVALID_ARG;
+  if (s->tokens < 0 || (s->tokens > 1 && s->batch % s->tokens != 0)) return CSA2_ERR_INVALID_ARG;
   if (s->n_entries > (1 << 28) || s->batch > (1 << 20)) return CSA2_ERR_UNSUPPORTED;
   if (s->idx_heads > 64 || s->idx_dim > 1024 || s->idx_heads * s->idx_dim > 8192) return CSA2_ERR_UNSUPPORTED;
   if (s->topk > 1024 || s->swa > 1024 || s->topk + s->swa > 1024) return CSA2_ERR_UNSUPPORTED;
@@ -97,6 +98,9 @@ int check_shape(const csa2_shape* s) {
   if (s->pool_blocks > topk_max_chunk() / 2) return CSA2_ERR_UNSUPPORTED;
   return CSA2_OK;
 }
+
+// Queries per cache sequence (csa2_shape.tokens; 0 means 1).
+int seqdiv(const csa2_shape& s) { return s.tokens > 1 ? s.tokens : 1; }
 
 bool indexer_fast(const csa2_shape& s) { return s.dtype == CSA2_BF16 && s.idx_heads == 8 && s.idx_dim == 64; }
 bool pooled_fast(const csa2_shape& s) { return indexer_fast(s) && s.block == 8; }
@@ -123,12 +127,13 @@ float softmax_scale(const csa2_shape& s) { return s.scale > 0.f ? s.scale : 1.0f
 
 // ---------------------------------------------------------------- internal ops (no validation)
 
-int do_index_flat(const csa2_shape& s, const void* q_idx, const float* w, const void* keys, int64_t rows_per_seq,
+int do_index_flat(const csa2_shape& s, const void* q_idx, const float* w, const void* keys, int64_t rows_per_seq, int seq_div,
                   const int32_t* n_valid, int div, float* scores, int32_t* cand, int32_t* n_cand, int64_t ld,
                   int* err, cudaStream_t st) {
   IndexerArgs a{};
   a.keys = keys;
   a.rows_per_seq = rows_per_seq;
+  a.seq_div = seq_div;
   a.q_idx = q_idx;
   a.w = w;
   a.n_valid = n_valid;
@@ -154,6 +159,7 @@ int do_index_pooled(const csa2_shape& s, const void* q_idx, const float* w, cons
   IndexerArgs a{};
   a.keys = k_idx;
   a.rows_per_seq = s.n_entries;
+  a.seq_div = seqdiv(s);
   a.q_idx = q_idx;
   a.w = w;
   a.n_valid = n_valid;
@@ -227,6 +233,7 @@ int do_attn(const csa2_shape& s, const void* q, const void* k_main, const void* 
   a.q = q;
   a.k_main = k_main;
   a.v_main = v_main;
+  a.seq_div = seqdiv(s);
   a.idx = idx;
   a.k_swa = k_swa;
   a.v_swa = v_swa;
@@ -246,12 +253,13 @@ int do_attn(const csa2_shape& s, const void* q, const void* k_main, const void* 
   return cuda_status(launch_attn(a, attn_fast(s), s.batch, st));
 }
 
-SelectArgs select_args(const csa2_shape& s, const void* keys, int64_t rows_per_seq, const void* q_idx,
+SelectArgs select_args(const csa2_shape& s, const void* keys, int64_t rows_per_seq, int seq_div, const void* q_idx,
                        const float* w, const int32_t* n_valid, int div, int k, int32_t* out, int64_t ld_out,
                        int32_t* n_out, int* err) {
   SelectArgs a{};
   a.keys = keys;
   a.rows_per_seq = rows_per_seq;
+  a.seq_div = seq_div;
   a.q_idx = q_idx;
   a.w = w;
   a.relu = s.relu;
@@ -272,13 +280,13 @@ int do_index_blocks(const csa2_shape& s, const WsLayout& L, void* ws, const void
   int* err = at<int>(ws, L.hdr);
   if (indexer_fast(s) && index_select_supported(false, int(L.nb_cap))) {
     // fused: block scoring and pool selection in one cluster launch
-    SelectArgs a = select_args(s, kb, L.nb_cap, q_idx, w, n_valid, s.block, s.pool_blocks, pool_out,
+    SelectArgs a = select_args(s, kb, L.nb_cap, 1, q_idx, w, n_valid, s.block, s.pool_blocks, pool_out,
                                s.pool_blocks, n_pool_out, err);
     return cuda_status(launch_index_select(a, false, s.batch, int(L.nb_cap), st));
   }
   float* bs = at<float>(ws, L.blk_scores);
   int32_t* nblk = at<int32_t>(ws, L.n_blk);
-  CSA2_TRY(do_index_flat(s, q_idx, w, kb, L.nb_cap, n_valid, s.block, bs, nullptr, nblk, L.nb_cap, err, st));
+  CSA2_TRY(do_index_flat(s, q_idx, w, kb, L.nb_cap, 1, n_valid, s.block, bs, nullptr, nblk, L.nb_cap, err, st));
   return do_topk(s, L, ws, bs, L.nb_cap, nullptr, nblk, L.nb_cap, s.pool_blocks, pool_out, nullptr, n_pool_out,
                  st);
 }
@@ -323,6 +331,7 @@ int csa2_block_keys(const csa2_shape* shape, const void* k_idx, const int32_t* n
   const WsLayout L = layout(s);
   BlockKeyArgs a{};
   a.k_idx = k_idx;
+  a.seq_div = seqdiv(s);
   a.n_valid = n_valid;
   a.kb = kb;
   a.n_entries = s.n_entries;
@@ -341,6 +350,7 @@ int csa2_kv_append(const csa2_shape* shape, int32_t max_new, const int32_t* n_ne
   CSA2_TRY(check_shape(shape));
   const csa2_shape& s = *shape;
   CSA2_TRY(check_ws(s, ws, ws_bytes));
+  if (seqdiv(s) != 1) return CSA2_ERR_UNSUPPORTED;   // appends are per sequence: pass a one-token shape
   if (max_new < 0 || max_new > s.n_entries) return CSA2_ERR_INVALID_ARG;
   if (n_new == nullptr || n_valid == nullptr || k_main == nullptr || v_main == nullptr || k_idx == nullptr)
     return CSA2_ERR_INVALID_ARG;
@@ -375,6 +385,7 @@ int csa2_swa_append(const csa2_shape* shape, const csa2_swa_slot* layers, int32_
   CSA2_TRY(check_shape(shape));
   const csa2_shape& s = *shape;
   CSA2_TRY(check_ws(s, ws, ws_bytes));
+  if (seqdiv(s) != 1) return CSA2_ERR_UNSUPPORTED;   // rings are per query: pass a one-token shape
   if (s.swa < 1 || layers == nullptr || n_layers < 1 || n_layers > kMaxSwaLayers) return CSA2_ERR_INVALID_ARG;
   if (swa_head == nullptr || n_swa == nullptr) return CSA2_ERR_INVALID_ARG;
   const WsLayout L = layout(s);
@@ -423,7 +434,7 @@ int csa2_index_tokens(const csa2_shape* shape, const void* q_idx, const float* w
   const WsLayout L = layout(s);
   int* err = at<int>(ws, L.hdr);
   if (pool == nullptr)
-    return do_index_flat(s, q_idx, w, k_idx, s.n_entries, n_valid, 1, scores_out, cand_out, n_cand_out,
+    return do_index_flat(s, q_idx, w, k_idx, s.n_entries, seqdiv(s), n_valid, 1, scores_out, cand_out, n_cand_out,
                          s.n_entries, err, stream);
   if (s.pool_blocks < 1 || n_pool == nullptr || cand_out == nullptr || n_cand_out == nullptr)
     return CSA2_ERR_INVALID_ARG;
@@ -449,15 +460,15 @@ int csa2_index_topk(const csa2_shape* shape, const void* q_idx, const float* w, 
   int32_t* nc = at<int32_t>(ws, L.n_cand);
   if (pool == nullptr) {
     if (indexer_fast(s) && index_select_supported(false, s.n_entries)) {
-      SelectArgs a = select_args(s, k_idx, s.n_entries, q_idx, w, n_valid, 1, k, idx_out, k, n_out, err);
+      SelectArgs a = select_args(s, k_idx, s.n_entries, seqdiv(s), q_idx, w, n_valid, 1, k, idx_out, k, n_out, err);
       return cuda_status(launch_index_select(a, false, s.batch, s.n_entries, stream));
     }
-    CSA2_TRY(do_index_flat(s, q_idx, w, k_idx, s.n_entries, n_valid, 1, ts, nullptr, nc, s.n_entries, err, stream));
+    CSA2_TRY(do_index_flat(s, q_idx, w, k_idx, s.n_entries, seqdiv(s), n_valid, 1, ts, nullptr, nc, s.n_entries, err, stream));
     return do_topk(s, L, ws, ts, s.n_entries, nullptr, nc, s.n_entries, k, idx_out, nullptr, n_out, stream);
   }
   if (s.pool_blocks < 1 || n_pool == nullptr || s.n_entries % s.block != 0) return CSA2_ERR_INVALID_ARG;
   if (pooled_fast(s) && index_select_supported(true, s.pool_blocks)) {
-    SelectArgs a = select_args(s, k_idx, s.n_entries, q_idx, w, n_valid, 1, k, idx_out, k, n_out, err);
+    SelectArgs a = select_args(s, k_idx, s.n_entries, seqdiv(s), q_idx, w, n_valid, 1, k, idx_out, k, n_out, err);
     a.pool = pool;
     a.n_pool = n_pool;
     a.pool_cap = s.pool_blocks;
@@ -554,7 +565,7 @@ int csa2_layer_group(const csa2_shape* shape, const csa2_layer* layers, int32_t 
         CSA2_TRY(do_index_blocks(s, L, ws, y.q_idx, y.w_idx, kb, n_valid, pool, npool, stream));
         if (pooled_fast(s) && index_select_supported(true, s.pool_blocks)) {
           // fused: pooled token scoring and Top-K in one cluster launch
-          SelectArgs a = select_args(s, k_idx, s.n_entries, y.q_idx, y.w_idx, n_valid, 1, s.topk, dst, s.topk,
+          SelectArgs a = select_args(s, k_idx, s.n_entries, seqdiv(s), y.q_idx, y.w_idx, n_valid, 1, s.topk, dst, s.topk,
                                      nullptr, err);
           a.pool = pool;
           a.n_pool = npool;
@@ -567,11 +578,11 @@ int csa2_layer_group(const csa2_shape* shape, const csa2_layer* layers, int32_t 
         }
       } else if (indexer_fast(s) && index_select_supported(false, s.n_entries)) {
         // fused: flat token scoring and Top-K in one cluster launch
-        SelectArgs a = select_args(s, k_idx, s.n_entries, y.q_idx, y.w_idx, n_valid, 1, s.topk, dst, s.topk,
+        SelectArgs a = select_args(s, k_idx, s.n_entries, seqdiv(s), y.q_idx, y.w_idx, n_valid, 1, s.topk, dst, s.topk,
                                    nullptr, err);
         CSA2_TRY(cuda_status(launch_index_select(a, false, s.batch, s.n_entries, stream)));
       } else {
-        CSA2_TRY(do_index_flat(s, y.q_idx, y.w_idx, k_idx, s.n_entries, n_valid, 1, ts, nullptr, nc, s.n_entries,
+        CSA2_TRY(do_index_flat(s, y.q_idx, y.w_idx, k_idx, s.n_entries, seqdiv(s), n_valid, 1, ts, nullptr, nc, s.n_entries,
                                err, stream));
         CSA2_TRY(do_topk(s, L, ws, ts, s.n_entries, nullptr, nc, s.n_entries, s.topk, dst, nullptr, nullptr,
                          stream));

@@ -168,7 +168,7 @@ __global__ void __launch_bounds__(kThreads, 2) attn_mma_kernel(const AttnArgs a)
         } else {
           if (e >= a.n_entries) report(a.err, kErrBadIndex, e);
           ok = e >= 0 && e < a.n_entries;
-          const long long row = (long long)b * a.n_entries + e;
+          const long long row = (long long)(b / a.seq_div) * a.n_entries + e;
           kr = static_cast<const uint8_t*>(a.k_main) + row * (kDk * 2);
           vr = static_cast<const uint8_t*>(a.v_main) + row * (kDv * 2);
         }
@@ -357,7 +357,7 @@ __global__ void __launch_bounds__(128) attn_generic_kernel(const AttnArgs a) {
       if (e >= a.n_entries && h == 0) report(a.err, kErrBadIndex, e);
       if (e >= 0 && e < a.n_entries) {
         kb = a.k_main;
-        r = (long long)b * a.n_entries + e;
+        r = (long long)(b / a.seq_div) * a.n_entries + e;
       }
     } else if (j - a.topk < ns) {
       kb = a.k_swa;
@@ -398,7 +398,7 @@ __global__ void __launch_bounds__(128) attn_generic_kernel(const AttnArgs a) {
       const void* vb;
       if (j < a.topk) {
         vb = a.v_main;
-        r = (long long)b * a.n_entries + a.idx[(long long)b * a.topk + j];
+        r = (long long)(b / a.seq_div) * a.n_entries + a.idx[(long long)b * a.topk + j];
       } else {
         vb = a.v_swa;
         r = (long long)b * a.swa + (j - a.topk);

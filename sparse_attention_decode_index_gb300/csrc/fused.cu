@@ -187,7 +187,7 @@ __global__ void __launch_bounds__(kThreads, 4) index_select_kernel(const SelectA
   // ---------------- phase 1: stream and score (keys -> s_key)
   uint32_t my_cnt = 0u, my_lo = 0xffffffffu, my_hi = 0u;   // this thread's keys
   const int ntiles = (rows_total + kTileRows - 1) / kTileRows;
-  const uint8_t* keys = static_cast<const uint8_t*>(a.keys) + (long long)b * a.rows_per_seq * kRowBytes;
+  const uint8_t* keys = static_cast<const uint8_t*>(a.keys) + (long long)(b / a.seq_div) * a.rows_per_seq * kRowBytes;
   if (warp == kConsumers) {
     int i = 0;
     for (; i < ntiles; ++i) {

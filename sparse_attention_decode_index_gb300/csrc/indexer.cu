@@ -95,7 +95,7 @@ __global__ void __launch_bounds__(kThreads) indexer_mma_kernel(const IndexerArgs
 
   const int rows_total = POOLED ? (end - begin) * kBlock : (end - begin);
   const int ntiles = (rows_total + kTileRows - 1) / kTileRows;
-  const uint8_t* keys = static_cast<const uint8_t*>(a.keys) + (long long)b * a.rows_per_seq * kRowBytes;
+  const uint8_t* keys = static_cast<const uint8_t*>(a.keys) + (long long)(b / a.seq_div) * a.rows_per_seq * kRowBytes;
 
   if (warp == kConsumers) {
     // ---------------- producer warp
@@ -252,7 +252,7 @@ __global__ void __launch_bounds__(256) indexer_generic_kernel(const IndexerArgs 
   }
   float s = -__int_as_float(0x7f800000);
   if (cand_id >= 0) {
-    const long long base = ((long long)b * a.rows_per_seq + row) * a.dim;
+    const long long base = ((long long)(b / a.seq_div) * a.rows_per_seq + row) * a.dim;
     s = 0.f;
     for (int h = 0; h < a.heads; ++h) {
       float d = 0.f;
@@ -274,7 +274,7 @@ __global__ void __launch_bounds__(256) block_keys_kernel(const BlockKeyArgs a) {
   if (i >= (long long)a.nb_cap * a.dim) return;
   const int j = int(i / a.dim), d = int(i % a.dim);
   const int nv = clamp_count(a.n_valid[b], a.n_entries, a.err);
-  const float v = block_key_elem(a.k_idx, (long long)b * a.n_entries, a.dim, a.block, nv, j, d, a.dtype,
+  const float v = block_key_elem(a.k_idx, (long long)(b / a.seq_div) * a.n_entries, a.dim, a.block, nv, j, d, a.dtype,
                                  a.round_to_int);
   store_elem(a.kb, ((long long)b * a.nb_cap + j) * a.dim + d, a.dtype, v);
 }

@@ -15,8 +15,9 @@ constexpr int kErrBadPool = 8;    // a pooled block id outside [0, ceil(n_valid 
 // Indexer scoring: s = sum_h w_h * ReLU(q_h . k) over a flat row range or the
 // entries of pooled blocks.
 struct IndexerArgs {
-  const void* keys;          // [B, rows_per_seq, dim] (indexer keys or block keys)
+  const void* keys;          // [B / seq_div, rows_per_seq, dim] (indexer keys or block keys)
   long long rows_per_seq;    // row capacity per sequence
+  int seq_div;               // queries per key sequence: query b reads sequence b / seq_div
   const void* q_idx;         // [B, heads, dim]
   const float* w;            // [B, heads]
   const int* n_valid;        // [B] valid compressed entries per query
@@ -53,8 +54,9 @@ struct TopkArgs {
 
 struct AttnArgs {
   const void* q;             // [B, H, dk]
-  const void* k_main;        // [B, N, dk]
-  const void* v_main;        // [B, N, dv]
+  const void* k_main;        // [B / seq_div, N, dk]
+  const void* v_main;        // [B / seq_div, N, dv]
+  int seq_div;               // queries per KV sequence: query b reads sequence b / seq_div
   const int* idx;            // [B, topk]
   const void* k_swa;         // [B, W, dk]
   const void* v_swa;         // [B, W, dv]
@@ -71,8 +73,9 @@ struct AttnArgs {
 // Fused scoring + cluster Top-k (fused.cu): one cluster per query scores its
 // candidates and writes the selected ids (ascending, -1 padded).
 struct SelectArgs {
-  const void* keys;          // [B, rows_per_seq, 64] bf16 (indexer keys or block keys)
+  const void* keys;          // [B / seq_div, rows_per_seq, 64] bf16 (indexer keys or block keys)
   long long rows_per_seq;
+  int seq_div;               // queries per key sequence: query b reads sequence b / seq_div
   const void* q_idx;         // [B, 8, 64] bf16
   const float* w;            // [B, 8]
   int relu;
@@ -94,9 +97,10 @@ bool index_select_supported(bool pooled, int max_units);
 cudaError_t launch_index_select(const SelectArgs& a, bool pooled, int batch, int max_units, cudaStream_t st);
 
 struct BlockKeyArgs {
-  const void* k_idx;         // [B, N, dim]
-  const int* n_valid;        // [B]
-  void* kb;                  // [B, NB, dim]
+  const void* k_idx;         // [B / seq_div, N, dim]
+  const int* n_valid;        // [B] (per query)
+  void* kb;                  // [B, NB, dim] (per query)
+  int seq_div;               // queries per key sequence
   int n_entries, nb_cap, dim, block, round_to_int, dtype;
   int* err;
 };

@@ -73,6 +73,7 @@ class Shape:
     scale: float = 0.0    # 0 -> 1/sqrt(k_dim)
     relu: int = 1
     dtype: str = "bf16"   # "bf16" or "f32"
+    tokens: int = 1       # query tokens per sequence: the caches are [batch / tokens, n_entries, ...]
 
     @property
     def softmax_scale(self) -> float:
@@ -184,6 +185,7 @@ def make_workload(shape: Shape, modes: List[int], *, seed: int = 0, cfg_id: int 
     the full capacity; pass arrays (or callables of the rng) for ragged cases.
     """
     B, N = shape.batch, shape.n_entries
+    S = B // max(1, shape.tokens)     # cache sequences
     f32 = shape.dtype == "f32"
 
     def kv(key, shp, d):
@@ -197,9 +199,9 @@ def make_workload(shape: Shape, modes: List[int], *, seed: int = 0, cfg_id: int 
             return _draw(shp, key, "normal", 1.0, bf16=not f32)
         return _draw(shp, key, "int")
 
-    k_main = kv((seed, cfg_id, 1), (B, N, shape.k_dim), shape.k_dim)
-    v_main = kv((seed, cfg_id, 2), (B, N, shape.v_dim), shape.v_dim)
-    k_idx = idxv((seed, cfg_id, 3), (B, N, shape.idx_dim))
+    k_main = kv((seed, cfg_id, 1), (S, N, shape.k_dim), shape.k_dim)
+    v_main = kv((seed, cfg_id, 2), (S, N, shape.v_dim), shape.v_dim)
+    k_idx = idxv((seed, cfg_id, 3), (S, N, shape.idx_dim))
     if n_valid is None:
         n_valid = np.full(B, N, dtype=np.int32)
     if n_swa is None:
@@ -225,6 +227,38 @@ def make_workload(shape: Shape, modes: List[int], *, seed: int = 0, cfg_id: int 
                     n_valid=np.asarray(n_valid, dtype=np.int32),
                     n_swa=np.asarray(n_swa, dtype=np.int32), layers=layers,
                     round_block_keys=round_block_keys)
+
+
+def decoder_replay(sequences: int, tokens: int, context: int, *, n_entries: int, pool: int, modes: List[int],
+                   seed: int = 0, cfg_id: int = 6, ratio: int = 4, name: str = "replay") -> Workload:
+    """The last ``tokens`` prompt tokens of each sequence run through a decoder
+    group together (architecture page, "Asymmetric encoder-decoder": a
+    128-token decoder replay).  Token t of a sequence sits at position
+    p = context - tokens + t.  It sees the compressed entries that end at or
+    before p, (p + 1) // ratio of them, and an SWA window of its own last
+    min(W, p + 1) raw tokens, oldest first.  The windows of consecutive tokens
+    are slices of one raw-token K/V stream per sequence, so they overlap as
+    they do in a model.  Caches are per sequence, everything else per token.
+    """
+    B = sequences * tokens
+    shape = Shape(batch=B, n_entries=n_entries, pool_blocks=pool, tokens=tokens)
+    W = shape.swa
+    pos = context - tokens + np.arange(tokens)
+    n_valid = np.tile(np.minimum((pos + 1) // ratio, n_entries), sequences).astype(np.int32)
+    n_swa = np.tile(np.minimum(W, pos + 1), sequences).astype(np.int32)
+    wl = make_workload(shape, modes, seed=seed, cfg_id=cfg_id, n_valid=n_valid, n_swa=n_swa, name=name)
+    span = tokens + W - 1                       # raw tokens covered by all windows of a sequence
+    for l, L in enumerate(wl.layers):
+        raw_k = _draw((sequences, span, shape.k_dim), (seed, cfg_id, 20, l), "normal", float(np.sqrt(shape.k_dim)))
+        raw_v = _draw((sequences, span, shape.v_dim), (seed, cfg_id, 21, l), "normal", float(np.sqrt(shape.v_dim)))
+        for s_ in range(sequences):
+            for t in range(tokens):
+                b = s_ * tokens + t
+                n = int(n_swa[b])                # window rows: raw positions p - n + 1 .. p
+                L.k_swa[b, :n] = raw_k[s_, t + W - n: t + W]
+                L.v_swa[b, :n] = raw_v[s_, t + W - n: t + W]
+    wl.note = f"{sequences} x {tokens} replayed tokens at {context} tokens, ratio {ratio}"
+    return wl
 
 
 def toy16(seed: int = 0) -> Workload:
@@ -266,6 +300,9 @@ WORKLOADS = {
                               context=32768),
     "dec_b16_1m": dict(cfg_id=4, batch=16, n_entries=262144, modes=decoder_group_modes(),
                        pool=2048, context=1048576),
+    # one sequence's 128-token decoder replay through the 20-layer decoder group at 128K context
+    "replay_t128_128k": dict(cfg_id=6, sequences=1, tokens=128, n_entries=32768, modes=decoder_group_modes(),
+                             pool=2048, context=131072),
 }
 
 
@@ -274,6 +311,9 @@ def named(name: str, seed: int = 0, batch: Optional[int] = None) -> Workload:
     if name == "toy16":
         return toy16(seed)
     spec = WORKLOADS[name]
+    if "tokens" in spec:
+        return decoder_replay(spec["sequences"], spec["tokens"], spec["context"], n_entries=spec["n_entries"],
+                              pool=spec["pool"], modes=spec["modes"], seed=seed, cfg_id=spec["cfg_id"], name=name)
     shape = Shape(batch=batch or spec["batch"], n_entries=spec["n_entries"],
                   pool_blocks=spec["pool"])
     wl = make_workload(shape, spec["modes"], seed=seed, cfg_id=spec["cfg_id"], name=name)

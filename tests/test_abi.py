@@ -142,6 +142,20 @@ def test_append_entry_points_reject_bad_arguments_before_launch(csa2):
     assert swa(s, sl=ctypes.cast(bad, ctypes.c_void_p)) == INVALID
 
 
+def test_tokens_per_sequence_rules(csa2):
+    lib = csa2.lib()
+    bad = csa2.c_shape(_shape(batch=6, tokens=4))                  # 6 queries are not whole sequences of 4
+    assert lib.csa2_workspace_bytes(ctypes.byref(bad)) == 0
+    s = csa2.c_shape(_shape(batch=8, tokens=4))
+    wsb = lib.csa2_workspace_bytes(ctypes.byref(s))
+    assert wsb > 0
+    UNSUP = -2
+    assert lib.csa2_kv_append(ctypes.byref(s), 1, *([FAKE] * 9), 1, FAKE, wsb, None) == UNSUP
+    slot = (csa2.CSwaSlot * 1)(csa2.CSwaSlot(FAKE, FAKE, FAKE, FAKE))
+    assert lib.csa2_swa_append(ctypes.byref(s), ctypes.cast(slot, ctypes.c_void_p), 1, FAKE, FAKE, FAKE, wsb,
+                               None) == UNSUP
+
+
 def _layers(csa2, modes, hier=None):
     arr = (csa2.CLayer * len(modes))()
     for i, m in enumerate(modes):

@@ -193,3 +193,14 @@ def test_swa_layers_anywhere_in_a_group(csa2):
                       n_swa=[128, 0, 5, 128, 1, 64], pool=32)
     d = run_gpu(csa2, wl)
     check_group(csa2, wl, d)
+
+
+@pytest.mark.parametrize("modes", [[FULL, REINDEX, REUSE], [SWA, REINDEX, REUSE, FULL]])
+def test_several_tokens_per_sequence_share_the_caches(csa2, modes):
+    """A decoder replay: 2 sequences x 16 consecutive tokens, caches shared per sequence,
+    each token with its own causal n_valid (ragged within the last blocks), its own
+    sliding window and its own block summary keys."""
+    wl = W.decoder_replay(2, 16, 8192, n_entries=2048, pool=64, modes=modes, seed=7)
+    assert wl.k_main.shape[0] == 2 and wl.shape.batch == 32
+    d = run_gpu(csa2, wl)
+    check_group(csa2, wl, d)

@@ -405,3 +405,27 @@ def test_attention_over_the_ring_equals_attention_oldest_first():
     b = oracle.sparse_attention(q, k_main, v_main, idx, k_old[ring], v_old[ring], Wn, 0.4)
     np.testing.assert_allclose(a[0], b[0], rtol=0, atol=1e-12)
     np.testing.assert_allclose(a[1], b[1], rtol=0, atol=1e-12)
+
+
+# ---------------------------------------------------------------- several tokens per sequence
+
+def test_decoder_replay_shares_caches_and_slides_the_windows():
+    """With T tokens per sequence the oracle reads sequence b // T; copying that
+    sequence's caches to every query gives the same result.  The workload's
+    windows slide by one raw token per query, and n_valid is causal at ratio 4."""
+    T = 8
+    wl = W.decoder_replay(2, T, 1000, n_entries=256, pool=8, modes=[FULL, REINDEX, REUSE], seed=1)
+    pos = 1000 - T + np.arange(T)
+    assert wl.n_valid.tolist() == list((pos + 1) // 4) * 2
+    for L in wl.layers:
+        for b in range(2 * T - 1):
+            if b % T != T - 1:        # consecutive tokens of one sequence: the window moves by one row
+                assert np.array_equal(L.k_swa[b, 1:], L.k_swa[b + 1, :-1])
+    import dataclasses
+    rep = lambda a: np.repeat(a, T, axis=0)
+    flat = dataclasses.replace(wl, shape=dataclasses.replace(wl.shape, tokens=1), k_main=rep(wl.k_main),
+                               v_main=rep(wl.v_main), k_idx=rep(wl.k_idx))
+    qs = [0, 3, 9, 15]
+    a, b = oracle.run_group(wl, queries=qs), oracle.run_group(flat, queries=qs)
+    for x, y in zip(a, b):
+        assert np.array_equal(x["idx"], y["idx"]) and np.array_equal(x["out"], y["out"])
