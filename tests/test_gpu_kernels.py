@@ -307,3 +307,40 @@ def test_index_topk_fused(csa2, mode):
             assert got[b].tolist() == r["idx"].tolist(), f"{mode} k={k} query {b}"
             assert int(n_out.cpu().numpy()[b]) == int((r["idx"] >= 0).sum())
     assert_no_device_error(csa2, ws)
+
+
+@pytest.mark.parametrize("case", ["outlier", "relu_off"])
+def test_index_topk_pooled_wide_or_negative_scores(csa2, case):
+    """Pooled scoring + Top-k when the 256 fixed bins below the top score hold fewer than
+    k keys (one score 2**100 times the rest: the first pass is redone over [min, max]),
+    and with ReLU off, where most scores are negative."""
+    rng = np.random.default_rng(31)
+    B, N, P, K = 3, 4096, 64, 256
+    sh = _shape(batch=B, n_entries=N, pool_blocks=P, topk=K, relu=0 if case == "relu_off" else 1)
+    k_idx = _int_keys(rng, (B, N, sh.idx_dim))
+    if case == "outlier":
+        big = W.f32_to_bf16_bits(np.array([2.0 ** 100], dtype=np.float32))[0]
+        for b in range(B):
+            k_idx[b, 1000 + 37 * b] = big                    # every dim 2**100: score ~2**100 times the rest
+    q_idx = _int_keys(rng, (B, sh.idx_heads, sh.idx_dim))
+    if case == "outlier":
+        q_idx[:, :, :] = W.f32_to_bf16_bits(np.array([1.0], dtype=np.float32))[0]   # positive dot products
+    w = rng.integers(1, 4, size=(B, sh.idx_heads)).astype(np.float32)
+    n_valid = np.array([N, N - 11, 3000], dtype=np.int32)
+    ws = csa2.workspace(sh)
+    kb = torch.zeros((B, N // 8, sh.idx_dim), dtype=torch.bfloat16, device="cuda")
+    csa2.block_keys(sh, bf16(k_idx), i32(n_valid), kb, ws, round_to_int=True)
+    pool = torch.zeros((B, P), dtype=torch.int32, device="cuda")
+    n_pool = torch.zeros(B, dtype=torch.int32, device="cuda")
+    csa2.index_blocks(sh, bf16(q_idx), f32(w), kb, i32(n_valid), pool, n_pool, ws)
+    idx = torch.full((B, K), -9, dtype=torch.int32, device="cuda")
+    csa2.index_topk(sh, bf16(q_idx), f32(w), bf16(k_idx), i32(n_valid), K, idx, ws, pool=pool, n_pool=n_pool)
+    got = idx.cpu().numpy()
+    for b in range(B):
+        keys = oracle.to_f64(k_idx[b])
+        n = int(n_valid[b])
+        kb_o = oracle.block_keys(keys, n, 8, True)
+        r = oracle.layer_indices(oracle.to_f64(q_idx[b]), w[b].astype(np.float64), keys, kb_o, n, topk=K,
+                                 block=8, pool=P, hier=True, relu=case != "relu_off")
+        assert got[b].tolist() == r["idx"].tolist(), f"{case} query {b}"
+    assert_no_device_error(csa2, ws)
