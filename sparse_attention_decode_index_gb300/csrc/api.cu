@@ -80,8 +80,6 @@ T* at(void* ws, size_t off) {
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
-int elem_bytes(const csa2_shape& s) { return s.dtype == CSA2_F32 ? 4 : 2; }
-
 int check_shape(const csa2_shape* s) {
   if (s == nullptr) return CSA2_ERR_INVALID_ARG;
   if (s->batch < 1 || s->n_entries < 1 || s->idx_heads < 1 || s->idx_dim < 1 || s->block < 1 ||
