@@ -304,24 +304,39 @@ __global__ void __launch_bounds__(kThreads, 2) attn_mma_kernel(const AttnArgs a)
     for (uint32_t r = 0; r < ncta; ++r) sW[r * kH + h] *= inv;
   }
   __syncthreads();
-  for (int e = tid; e < (he - hb) * (kDv / 4); e += kThreads) {
-    const int h = hb + e / (kDv / 4), d4 = e % (kDv / 4);
-    float4 v[kMaxCluster];
+  // Up to kItems (head, 4 columns) items per thread, all their partial loads issued
+  // before any is used (each item reads one float4 from every CTA of the cluster).
+  constexpr int kItems = 4;
+  const int n_items = (he - hb) * (kDv / 4);
+  for (int e0 = tid; e0 < n_items; e0 += kItems * kThreads) {
+    float4 v[kItems][kMaxCluster];
 #pragma unroll
-    for (int r = 0; r < kMaxCluster; ++r)
-      if (r < int(ncta))
-        v[r] = __ldcg(reinterpret_cast<const float4*>(a.part + ((size_t)(b * int(ncta) + r) * kH + h) * kDv + 4 * d4));
-    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int m = 0; m < kItems; ++m) {
+      const int e = e0 + m * kThreads;
+      const int h = hb + e / (kDv / 4), d4 = e % (kDv / 4);
 #pragma unroll
-    for (int r = 0; r < kMaxCluster; ++r)
-      if (r < int(ncta)) {
-        const float wr = sW[r * kH + h];
-        acc.x += wr * v[r].x;
-        acc.y += wr * v[r].y;
-        acc.z += wr * v[r].z;
-        acc.w += wr * v[r].w;
-      }
-    *reinterpret_cast<float4*>(a.out + ((long long)b * kH + h) * kDv + 4 * d4) = acc;
+      for (int r = 0; r < kMaxCluster; ++r)
+        if (e < n_items && r < int(ncta))
+          v[m][r] = __ldcg(reinterpret_cast<const float4*>(a.part + ((size_t)(b * int(ncta) + r) * kH + h) * kDv +
+                                                           4 * d4));
+    }
+#pragma unroll
+    for (int m = 0; m < kItems; ++m) {
+      const int e = e0 + m * kThreads;
+      if (e >= n_items) continue;
+      const int h = hb + e / (kDv / 4), d4 = e % (kDv / 4);
+      float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+      for (int r = 0; r < kMaxCluster; ++r)
+        if (r < int(ncta)) {
+          const float wr = sW[r * kH + h];
+          acc.x += wr * v[m][r].x;
+          acc.y += wr * v[m][r].y;
+          acc.z += wr * v[m][r].z;
+          acc.w += wr * v[m][r].w;
+        }
+      *reinterpret_cast<float4*>(a.out + ((long long)b * kH + h) * kDv + 4 * d4) = acc;
+    }
   }
   if (a.lse != nullptr && tid < he - hb) {
     const int h = hb + tid;
