@@ -20,7 +20,9 @@
 //   3. every CTA pushes its keys inside that bin into every CTA, which then
 //      finishes the selection alone (passes over the gathered keys, each
 //      narrowing to the exact [min, max] of the chosen bin) and counts each
-//      CTA's keys above and at the threshold.
+//      CTA's keys above and at the threshold.  The radix pass stores each
+//      key's bin as a byte, so finding the keys of the chosen bin compares
+//      bytes instead of binning every key again.
 //
 // Only while the chosen bin holds more keys than a CTA can gather do steps 1
 // and 2 repeat on the keys of that bin.  The first pass of each loop bins the
@@ -32,7 +34,8 @@
 // step waits on a remote load.  Ties at the threshold go to the lowest
 // indices: the CTAs hold ascending index ranges, so each CTA's quota and
 // output offset follow from the per-CTA counts, and each CTA writes its ids
-// directly in ascending order.
+// directly in ascending order (one pass lists each warp's keys at or above the
+// threshold, a second writes the ids from those short lists).
 //
 // (DeepSeek V4.1 Flash architecture page: bullet "Hierarchical indexer" -- block
 // pool, at most 16,384 candidates; bullet "Sparse attention" -- Top-512.)
@@ -60,7 +63,9 @@ constexpr int kMaxCluster = 8;
 constexpr int kMaxRowsPerCta = 4096;                 // order keys kept in shared memory
 // After scoring, the ring buffer is reused:
 //   region A: the histogram of a cluster-wide pass, two bins per word (16-bit
-//             counters, 32 lane-private copies), then the gather buffer;
+//             counters, 32 lane-private copies), then the gather buffer; its
+//             last kBinWords words hold the bin of every key of that pass
+//             (one byte per key), so that later tests need no binning;
 //   region B: the pushed per-CTA bin totals (two buffers), then the
 //             histogram (8 copies) and totals of the passes over gathered keys.
 constexpr int kRingWords = kStages * kTileBytes / 4;
@@ -69,8 +74,10 @@ constexpr int kHistDWords = (kBins / 2) * kLanes;
 constexpr int kGatherCap = kRingWords - 2 * kMaxCluster * kBins;   // words of region A
 constexpr int kTotWords = kMaxCluster * kBins;                      // one totals buffer
 constexpr int kCopiesL = 8;
+constexpr int kBinWords = kMaxRowsPerCta / 4;
+constexpr int kGatherWords = kGatherCap - kBinWords;                // gather buffer capacity
 
-static_assert(kHistDWords <= kGatherCap, "histogram fits region A");
+static_assert(kHistDWords <= kGatherWords, "histogram fits region A below the key bins");
 static_assert(kBins * kCopiesL + kBins <= 2 * kTotWords, "local histogram fits region B");
 static_assert(kMaxRowsPerCta < 65536, "16-bit histogram counters");
 
@@ -125,6 +132,21 @@ __device__ __forceinline__ uint32_t bin_of(uint32_t key, const Binning& bn) {
     return min(uint32_t(kBins - 1), __float2uint_rz(x));
   }
   return (key - bn.lo) >> bn.shift;
+}
+
+// Keys 4i .. 4i + 3 and 4(i + kThreads) .. 4(i + kThreads) + 3 of a key array of
+// nvec 16-byte vectors (i < nvec; zeros past the end).
+__device__ __forceinline__ void load_keys8(const uint4* kv, int i, int nvec, uint32_t (&kk)[8]) {
+  const uint4 x = kv[i];
+  const uint4 y = i + kThreads < nvec ? kv[i + kThreads] : make_uint4(0u, 0u, 0u, 0u);
+  kk[0] = x.x;
+  kk[1] = x.y;
+  kk[2] = x.z;
+  kk[3] = x.w;
+  kk[4] = y.x;
+  kk[5] = y.y;
+  kk[6] = y.z;
+  kk[7] = y.w;
 }
 
 constexpr size_t kOffSmall = size_t(kStages) * kTileBytes;
@@ -287,24 +309,28 @@ __global__ void __launch_bounds__(kThreads, 4) index_select_kernel(const SelectA
       }
     }
   }
+  if (tid < 3 && rows_total + tid < key_words(rows_total)) s_key[rows_total + tid] = 0u;   // padding: no candidate
   __syncthreads();   // all keys written; the ring buffer is free for the histogram
 
   // ---------------- phase 2: cluster-wide exact Top-k over the keys
   uint32_t* ring = reinterpret_cast<uint32_t*>(smem);
   uint32_t* histD = ring;                                 // [kBins / 2][kLanes], 16-bit pairs
   uint32_t* gk = ring;                                    // gathered keys, per-CTA segments
+  uint32_t* kbin = ring + kGatherWords;                   // [rows] bin of each key (bytes)
+  const uint8_t* kbin8 = reinterpret_cast<const uint8_t*>(kbin);
   uint32_t* tot = ring + kGatherCap;                      // [2][kMaxCluster][kBins]
   uint32_t* histL = tot;                                  // [kBins][kCopiesL]
   uint32_t* totL = tot + kBins * kCopiesL;                // [kBins]
   const uint32_t k = uint32_t(a.k);
+  const uint4* kv = reinterpret_cast<const uint4*>(s_key);   // 16-byte reads of the keys
+  const int nvec = key_words(rows_total) / 4;
   if (tid == 0) sm.gcount = 0u;
   if (tid < kMaxCluster) sm.above_r[tid] = 0u;
 
   // Selected: every key > T, plus the first q keys == T in index order.
   uint32_t T = 0u, q = 0u;
   uint32_t lo = 0u, hi = 0xffffffffu, need = k;
-  Binning flt{};                 // the members are the keys in [lo, hi] inside bin fsel of flt
-  uint32_t fsel = 0u;
+  uint32_t fsel = 0u;            // once filtered: the members are also in bin fsel of the last pass
   bool filtered = false, gathered = false, resolved = false;
   uint32_t n_all = 0u;           // valid candidates of the query
   for (int step = 0; step < 12 && !resolved; ++step) {
@@ -317,7 +343,7 @@ __global__ void __launch_bounds__(kThreads, 4) index_select_kernel(const SelectA
         h = 0u;
         for (int j = tid; j < rows_total; j += kThreads) {
           const uint32_t kk = s_key[j];
-          if (kk != 0u && kk >= lo && kk <= hi && (!filtered || bin_of(kk, flt) == fsel)) {
+          if (kk >= lo && kk <= hi && (!filtered || kbin8[j] == fsel)) {
             ++c;
             l = min(l, kk);
             h = max(h, kk);
@@ -391,16 +417,18 @@ __global__ void __launch_bounds__(kThreads, 4) index_select_kernel(const SelectA
 
     // (2) radix pass over [lo, hi]: every CTA's bin totals pushed to every CTA
     const Binning bn = make_binning(lo, hi, step == 0);
-    for (int j0 = tid; j0 < rows_total; j0 += 8 * kThreads) {
-      uint32_t kk[8];
+    for (int i0 = tid; i0 < nvec; i0 += 2 * kThreads) {
+      uint32_t kk[8], packed[2] = {0u, 0u};
+      load_keys8(kv, i0, nvec, kk);
 #pragma unroll
-      for (int u = 0; u < 8; ++u) kk[u] = j0 + u * kThreads < rows_total ? s_key[j0 + u * kThreads] : 0u;
-#pragma unroll
-      for (int u = 0; u < 8; ++u)
-        if (kk[u] != 0u && kk[u] >= lo && kk[u] <= hi) {
-          const uint32_t bin = bin_of(kk[u], bn);
-          atomicAdd(&histD[(bin >> 1) * kLanes + lane], (bin & 1u) ? 0x10000u : 1u);
-        }
+      for (int u = 0; u < 8; ++u) {   // no branch: a key outside [lo, hi] adds 0 to a clamped bin
+        const uint32_t bin = min(uint32_t(kBins - 1), bin_of(kk[u], bn));
+        const uint32_t inc = (kk[u] >= lo && kk[u] <= hi) ? ((bin & 1u) ? 0x10000u : 1u) : 0u;
+        atomicAdd(&histD[(bin >> 1) * kLanes + lane], inc);
+        packed[u >> 2] |= bin << (8 * (u & 3));
+      }
+      kbin[i0] = packed[0];
+      if (i0 + kThreads < nvec) kbin[i0 + kThreads] = packed[1];
     }
     __syncthreads();
     const int buf = step & 1;
@@ -474,12 +502,11 @@ __global__ void __launch_bounds__(kThreads, 4) index_select_kernel(const SelectA
     }
     __syncthreads();
     need -= sabove;
-    flt = bn;
     fsel = sel;
     filtered = true;
     uint32_t padded = 0u;
     for (int r = 0; r < int(ncta); ++r) padded += (sm.cnt_r[r] + 3u) & ~3u;
-    if (padded <= uint32_t(kGatherCap)) {
+    if (padded <= uint32_t(kGatherWords)) {
       gathered = true;
       resolved = true;
     }
@@ -494,16 +521,26 @@ __global__ void __launch_bounds__(kThreads, 4) index_select_kernel(const SelectA
       G += (sm.cnt_r[r] + 3u) & ~3u;
     }
     const uint32_t my_in = sm.cnt_r[crank];
-    for (int j0 = tid; j0 < rows_total; j0 += 8 * kThreads) {   // few keys match: one atomic each
-      uint32_t kk[8];
+    // members: keys in [lo, hi] whose bin byte is fsel; 16 bytes compared per read
+    const uint32_t sel4 = fsel * 0x01010101u;
+    const int nbv = (nvec + 3) >> 2;
+    for (int v = tid; v < nbv; v += kThreads) {   // few keys match: one atomic each
+      const uint4 w4 = reinterpret_cast<const uint4*>(kbin)[v];
+      const uint32_t w[4] = {w4.x, w4.y, w4.z, w4.w};
 #pragma unroll
-      for (int u = 0; u < 8; ++u) kk[u] = j0 + u * kThreads < rows_total ? s_key[j0 + u * kThreads] : 0u;
-#pragma unroll
-      for (int u = 0; u < 8; ++u)
-        if (kk[u] != 0u && kk[u] >= lo && kk[u] <= hi && bin_of(kk[u], flt) == fsel) {
-          const uint32_t p = atomicAdd(&sm.gcount, 1u);
-          if (p < my_in) gk[my_off + p] = kk[u];
+      for (int c = 0; c < 4; ++c) {
+        uint32_t m = __vcmpeq4(w[c], sel4);
+        while (m != 0u) {
+          const int byte = (__ffs(m) - 1) >> 3;
+          m &= ~(0xffu << (8 * byte));
+          const int j = 16 * v + 4 * c + byte;
+          const uint32_t kk = j < rows_total ? s_key[j] : 0u;
+          if (kk >= lo && kk <= hi) {
+            const uint32_t p = atomicAdd(&sm.gcount, 1u);
+            if (p < my_in) gk[my_off + p] = kk;
+          }
         }
+      }
     }
     if (tid < 3 && my_in + uint32_t(tid) < ((my_in + 3u) & ~3u)) gk[my_off + my_in + tid] = 0u;
     __syncthreads();
@@ -521,11 +558,14 @@ __global__ void __launch_bounds__(kThreads, 4) index_select_kernel(const SelectA
     // every CTA finishes the selection alone over the G gathered words (0 = padding)
     uint4* hl = reinterpret_cast<uint4*>(histL);
     bool done = false;
+    Binning lflt{};                // after the first pass: the members are also in bin lsel of lflt
+    uint32_t lsel = 0u;
+    bool lf = false;
     for (int it = 0; it < 12; ++it) {
       uint32_t mn = 0xffffffffu, mx = 0u, c = 0u;
       for (int i = tid; i < int(G); i += kThreads) {
         const uint32_t kk = gk[i];
-        if (kk != 0u && kk >= lo && kk <= hi && bin_of(kk, flt) == fsel) {
+        if (kk >= lo && kk <= hi && (!lf || bin_of(kk, lflt) == lsel)) {
           mn = min(mn, kk);
           mx = max(mx, kk);
           ++c;
@@ -601,8 +641,9 @@ __global__ void __launch_bounds__(kThreads, 4) index_select_kernel(const SelectA
       }
       __syncthreads();
       need -= sm.sel_above;
-      flt = bl;
-      fsel = sm.sel_bin;
+      lflt = bl;
+      lsel = sm.sel_bin;
+      lf = true;
     }
     if (!done) report(a.err, kErrBadCount, -3);   // cannot happen: every pass narrows the range
     // per CTA: gathered keys above and at the threshold
@@ -644,19 +685,28 @@ __global__ void __launch_bounds__(kThreads, 4) index_select_kernel(const SelectA
       eqb += sm.eq_r[r];
     }
   }
-  // each warp owns a contiguous run of positions; ballots give the ranks inside it
+  // Each warp owns a contiguous run of positions.  One pass lists, in order, the
+  // positions of the run's keys above or at the threshold (flagged) in the run's
+  // own stretch of a stage buffer (the ring is free now); the warps' counts give
+  // every warp its first output slot, and a pass over the short lists writes the ids.
+  uint32_t* stage = ring;
   const int seg = ((rows_total + kWarpsAll - 1) / kWarpsAll + 31) & ~31;
   const int p0 = warp * seg;
   const int p1 = min(rows_total, p0 + seg);
-  uint32_t wgt = 0u, weq = 0u;
+  const unsigned lt = (1u << lane) - 1u;
+  uint32_t wn = 0u, weq = 0u;
   for (int j0 = p0; j0 < p1; j0 += 32) {
     const int j = j0 + lane;
     const uint32_t kk = j < p1 ? s_key[j] : 0u;
-    wgt += uint32_t(__popc(__ballot_sync(0xffffffffu, kk > T)));
-    weq += uint32_t(__popc(__ballot_sync(0xffffffffu, q > 0u && kk == T)));
+    const bool eq = q > 0u && kk == T;
+    const bool hit = kk > T || eq;
+    const unsigned mh = __ballot_sync(0xffffffffu, hit);
+    if (hit) stage[p0 + wn + uint32_t(__popc(mh & lt))] = uint32_t(j) | (eq ? 0x80000000u : 0u);
+    wn += uint32_t(__popc(mh));
+    weq += uint32_t(__popc(__ballot_sync(0xffffffffu, eq)));
   }
   if (lane == 0) {
-    sm.red[0][warp] = wgt;
+    sm.red[0][warp] = wn - weq;
     sm.red[1][warp] = weq;
   }
   __syncthreads();
@@ -667,15 +717,15 @@ __global__ void __launch_bounds__(kThreads, 4) index_select_kernel(const SelectA
   }
   uint32_t slot = offset + gt_before + min(eq_before, quota);
   int* out = a.out + (long long)b * a.ld_out;
-  const unsigned lt = (1u << lane) - 1u;
-  for (int j0 = p0; j0 < p1; j0 += 32) {
-    const int j = j0 + lane;
-    const uint32_t kk = j < p1 ? s_key[j] : 0u;
-    const bool eq = q > 0u && kk == T;
+  for (uint32_t i0 = 0; i0 < wn; i0 += 32) {
+    const uint32_t i = i0 + uint32_t(lane);
+    const uint32_t v = i < wn ? stage[p0 + i] : 0u;
+    const bool eq = i < wn && (v & 0x80000000u) != 0u;
     const unsigned me = __ballot_sync(0xffffffffu, eq);
-    const bool take = kk > T || (eq && eq_before + uint32_t(__popc(me & lt)) < quota);
+    const bool take = i < wn && (!eq || eq_before + uint32_t(__popc(me & lt)) < quota);
     const unsigned mt = __ballot_sync(0xffffffffu, take);
     if (take) {
+      const int j = int(v & 0x7fffffffu);
       int id;
       if (!POOLED)
         id = begin + j;
