@@ -181,8 +181,8 @@ CSA2_DEV void dsmem_st_v2(uint32_t addr, float x, float y) {
   asm volatile("st.shared::cluster.v2.f32 [%0], {%1, %2};" ::"r"(addr), "f"(x), "f"(y) : "memory");
 }
 
-CSA2_DEV void dsmem_st_v2u(uint32_t addr, uint32_t x, uint32_t y) {
-  asm volatile("st.shared::cluster.v2.u32 [%0], {%1, %2};" ::"r"(addr), "r"(x), "r"(y) : "memory");
+CSA2_DEV void dsmem_st_u32(uint32_t addr, uint32_t x) {
+  asm volatile("st.shared::cluster.u32 [%0], %1;" ::"r"(addr), "r"(x) : "memory");
 }
 
 CSA2_DEV void dsmem_st_v4u(uint32_t addr, uint4 v) {

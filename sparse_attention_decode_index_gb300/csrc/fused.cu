@@ -49,10 +49,12 @@ namespace {
 constexpr int kHeads = 8;
 constexpr int kDim = 64;
 constexpr int kRowBytes = kDim * 2;
-constexpr int kTileRows = 128;
-constexpr int kTileBytes = kTileRows * kRowBytes;    // 16 KB
-constexpr int kStages = 3;
+constexpr int kTileRows = 64;
+constexpr int kTileBytes = kTileRows * kRowBytes;    // 8 KB
+constexpr int kStages = 5;
 constexpr int kConsumers = 4;
+constexpr int kMTiles = kTileRows / 16 / kConsumers; // 16-row MMA tiles per consumer warp and tile
+static_assert(kTileRows == 16 * kMTiles * kConsumers, "consumer warps split a tile evenly");
 constexpr int kThreads = (kConsumers + 1) * 32;      // 160
 constexpr int kWarpsAll = kThreads / 32;
 constexpr int kBlock = 8;
@@ -63,22 +65,26 @@ constexpr int kMaxCluster = 8;
 constexpr int kMaxRowsPerCta = 4096;                 // order keys kept in shared memory
 // After scoring, the ring buffer is reused:
 //   region A: the histogram of a cluster-wide pass, two bins per word (16-bit
-//             counters, 32 lane-private copies), then the gather buffer; its
-//             last kBinWords words hold the bin of every key of that pass
-//             (one byte per key), so that later tests need no binning;
-//   region B: the pushed per-CTA bin totals (two buffers), then the
-//             histogram (8 copies) and totals of the passes over gathered keys.
+//             counters, 32 lane-private copies), then the gather buffer;
+//             its tail first holds the bin of every key of the last pass (one
+//             byte per key, so that later tests need no binning), then the
+//             histogram (kCopiesL copies) and totals of the passes over the
+//             gathered keys;
+//   region B: the per-CTA bin totals pushed by every CTA, 16-bit counts two
+//             bins per word, in two buffers.
 constexpr int kRingWords = kStages * kTileBytes / 4;
 constexpr int kLanes = 32;
 constexpr int kHistDWords = (kBins / 2) * kLanes;
-constexpr int kGatherCap = kRingWords - 2 * kMaxCluster * kBins;   // words of region A
-constexpr int kTotWords = kMaxCluster * kBins;                      // one totals buffer
+constexpr int kTotWords = kMaxCluster * kBins / 2;                  // one totals buffer
+constexpr int kRegionA = kRingWords - 2 * kTotWords;
 constexpr int kCopiesL = 8;
+constexpr int kLocalWords = kBins * kCopiesL + kBins;               // local histogram + totals
 constexpr int kBinWords = kMaxRowsPerCta / 4;
-constexpr int kGatherWords = kGatherCap - kBinWords;                // gather buffer capacity
+constexpr int kGatherWords = kRegionA - kLocalWords;                // gather buffer capacity
 
-static_assert(kHistDWords <= kGatherWords, "histogram fits region A below the key bins");
-static_assert(kBins * kCopiesL + kBins <= 2 * kTotWords, "local histogram fits region B");
+static_assert(kHistDWords <= kGatherWords, "histogram fits region A below its tail");
+static_assert(kBinWords <= kLocalWords, "key bins fit the tail of region A");
+static_assert(kGatherWords % 4 == 0, "16-byte aligned tail");
 static_assert(kMaxRowsPerCta < 65536, "16-bit histogram counters");
 
 struct SelSmall {
@@ -257,10 +263,10 @@ __global__ void __launch_bounds__(kThreads, 4) index_select_kernel(const SelectA
       }
       const uint8_t* tile = tiles + s * kTileBytes;
       (void)tile;
-      uint32_t ra[2][8], rb[2][8];
+      uint32_t ra[kMTiles][8], rb[kMTiles][8];
 #pragma unroll
-      for (int m = 0; m < 2; ++m) {
-        const uint8_t* p = tile + ((warp * 2 + m) * 16 + g) * kRowBytes + 32 * t;
+      for (int m = 0; m < kMTiles; ++m) {
+        const uint8_t* p = tile + ((warp * kMTiles + m) * 16 + g) * kRowBytes + 32 * t;
         const uint4 x0 = *reinterpret_cast<const uint4*>(p);
         const uint4 x1 = *reinterpret_cast<const uint4*>(p + 16);
         const uint4 y0 = *reinterpret_cast<const uint4*>(p + 8 * kRowBytes);
@@ -273,7 +279,7 @@ __global__ void __launch_bounds__(kThreads, 4) index_select_kernel(const SelectA
       __syncwarp();
       if (lane == 0) mbar_arrive(&sm.empty[s]);
 #pragma unroll
-      for (int m = 0; m < 2; ++m) {
+      for (int m = 0; m < kMTiles; ++m) {
         float c0[4] = {0.f, 0.f, 0.f, 0.f}, c1[4] = {0.f, 0.f, 0.f, 0.f};
         mma_bf16(c0, ra[m][0], rb[m][0], ra[m][1], rb[m][1], qf[0], qf[1]);
         mma_bf16(c1, ra[m][2], rb[m][2], ra[m][3], rb[m][3], qf[2], qf[3]);
@@ -291,7 +297,7 @@ __global__ void __launch_bounds__(kThreads, 4) index_select_kernel(const SelectA
         r1 += __shfl_xor_sync(0xffffffffu, r1, 1);
         r0 += __shfl_xor_sync(0xffffffffu, r0, 2);
         r1 += __shfl_xor_sync(0xffffffffu, r1, 2);
-        const int row = i * kTileRows + (warp * 2 + m) * 16 + g + 8 * t;
+        const int row = i * kTileRows + (warp * kMTiles + m) * 16 + g + 8 * t;
         if (t < 2 && row < rows_total) {
           bool valid = true;
           if (POOLED) {
@@ -318,9 +324,9 @@ __global__ void __launch_bounds__(kThreads, 4) index_select_kernel(const SelectA
   uint32_t* gk = ring;                                    // gathered keys, per-CTA segments
   uint32_t* kbin = ring + kGatherWords;                   // [rows] bin of each key (bytes)
   const uint8_t* kbin8 = reinterpret_cast<const uint8_t*>(kbin);
-  uint32_t* tot = ring + kGatherCap;                      // [2][kMaxCluster][kBins]
-  uint32_t* histL = tot;                                  // [kBins][kCopiesL]
-  uint32_t* totL = tot + kBins * kCopiesL;                // [kBins]
+  uint32_t* histL = ring + kGatherWords;                  // [kBins][kCopiesL], after the gather
+  uint32_t* totL = histL + kBins * kCopiesL;              // [kBins]
+  uint32_t* tot = ring + kRegionA;                        // [2][kMaxCluster][kBins / 2]
   const uint32_t k = uint32_t(a.k);
   const uint4* kv = reinterpret_cast<const uint4*>(s_key);   // 16-byte reads of the keys
   const int nvec = key_words(rows_total) / 4;
@@ -437,8 +443,8 @@ __global__ void __launch_bounds__(kThreads, 4) index_select_kernel(const SelectA
       uint32_t sum = 0u;
 #pragma unroll 8
       for (int c = 0; c < kLanes; ++c) sum += row[(c + tid) & (kLanes - 1)];
-      uint32_t* dst = tot + buf * kTotWords + crank * kBins + 2 * tid;
-      for (int r = 0; r < int(ncta); ++r) dsmem_st_v2u(dsmem_addr(dst, uint32_t(r)), sum & 0xffffu, sum >> 16);
+      uint32_t* dst = tot + buf * kTotWords + crank * (kBins / 2) + tid;   // bins 2 tid, 2 tid + 1
+      for (int r = 0; r < int(ncta); ++r) dsmem_st_u32(dsmem_addr(dst, uint32_t(r)), sum);
     }
     cluster_sync_all();
     uint32_t sel, sabove;
@@ -447,13 +453,17 @@ __global__ void __launch_bounds__(kThreads, 4) index_select_kernel(const SelectA
       // 255 - 8l - j (j = 0..7), first their totals over the CTAs.
       const uint32_t* tb = tot + buf * kTotWords;
       const int b0 = kBins - 8 - 8 * lane;
-      uint32_t g[8] = {0u, 0u, 0u, 0u, 0u, 0u, 0u, 0u};
+      // packed sums over the CTAs: a 16-bit half never exceeds the cluster's keys (< 65,536)
+      uint4 s4 = make_uint4(0u, 0u, 0u, 0u);
       for (int r = 0; r < int(ncta); ++r) {
-        const uint4 x = *reinterpret_cast<const uint4*>(tb + r * kBins + b0);
-        const uint4 y = *reinterpret_cast<const uint4*>(tb + r * kBins + b0 + 4);
-        g[0] += y.w; g[1] += y.z; g[2] += y.y; g[3] += y.x;
-        g[4] += x.w; g[5] += x.z; g[6] += x.y; g[7] += x.x;
+        const uint4 x = *reinterpret_cast<const uint4*>(tb + r * (kBins / 2) + b0 / 2);   // bins b0 .. b0 + 7
+        s4.x += x.x;
+        s4.y += x.y;
+        s4.z += x.z;
+        s4.w += x.w;
       }
+      const uint32_t g[8] = {s4.w >> 16, s4.w & 0xffffu, s4.z >> 16, s4.z & 0xffffu,   // bin b0 + 7 - j
+                             s4.y >> 16, s4.y & 0xffffu, s4.x >> 16, s4.x & 0xffffu};
       uint32_t local = 0u;
 #pragma unroll
       for (int j = 0; j < 8; ++j) local += g[j];
@@ -482,9 +492,9 @@ __global__ void __launch_bounds__(kThreads, 4) index_select_kernel(const SelectA
       if (fm == 0u && tid == 0) report(a.err, kErrBadCount, -2);   // cannot happen: [lo, hi] holds >= need keys
       // then each CTA's keys above the chosen bin and inside it (CTA r by warp r mod 5)
       for (int r = warp; r < int(ncta); r += kWarpsAll) {
-        const uint4 x = *reinterpret_cast<const uint4*>(tb + r * kBins + b0);
-        const uint4 y = *reinterpret_cast<const uint4*>(tb + r * kBins + b0 + 4);
-        const uint32_t v[8] = {x.x, x.y, x.z, x.w, y.x, y.y, y.z, y.w};   // bins b0 .. b0 + 7
+        const uint4 x = *reinterpret_cast<const uint4*>(tb + r * (kBins / 2) + b0 / 2);
+        const uint32_t v[8] = {x.x & 0xffffu, x.x >> 16, x.y & 0xffffu, x.y >> 16,   // bins b0 .. b0 + 7
+                               x.z & 0xffffu, x.z >> 16, x.w & 0xffffu, x.w >> 16};
         uint32_t ab = 0u, in = 0u;
 #pragma unroll
         for (int j = 0; j < 8; ++j) {
@@ -668,11 +678,9 @@ __global__ void __launch_bounds__(kThreads, 4) index_select_kernel(const SelectA
     }
   }
   __syncthreads();
-
-  // Let the next launch in the stream start its CTAs only now: CTAs of the next
-  // kernel made resident earlier would sit on SM resources through this
-  // kernel's selection and slow its last clusters (measured: +12 us per step).
-  pdl_launch_dependents();
+  // The pooled stage lets the attention launch place its CTAs now: they fetch
+  // their SWA rows while this kernel writes its ids.
+  if (POOLED) pdl_launch_dependents();
 
   // ---------------- phase 3: this CTA's quota and offset, then its ids in ascending order
   uint32_t offset = 0u, quota = 0u;
@@ -741,6 +749,11 @@ __global__ void __launch_bounds__(kThreads, 4) index_select_kernel(const SelectA
     if (a.n_out != nullptr && tid == 0) a.n_out[b] = selected;
     for (int j = selected + tid; j < a.k; j += kThreads) out[j] = -1;
   }
+  // The block stage lets the next launch place its CTAs only now: with this
+  // kernel's small footprint, CTAs of the pooled stage would share SMs with its
+  // last clusters and slow them (measured per step: 2.5 us against a trigger
+  // before the output pass).
+  if (!POOLED) pdl_launch_dependents();
 }
 
 struct ClusterChoice {
