@@ -94,6 +94,8 @@ struct SelSmall {
   uint32_t cnt_r[kMaxCluster];     // per CTA: keys inside the current range
   uint32_t gt_r[kMaxCluster];      // per CTA: keys above the threshold
   uint32_t eq_r[kMaxCluster];      // per CTA: keys at the threshold
+  uint32_t gt_g[kMaxCluster];      // rank finish: per CTA, gathered keys above / at the threshold
+  uint32_t eq_g[kMaxCluster];
   uint32_t sel_bin, sel_above, gcount;
   uint64_t full[kStages];
   uint64_t empty[kStages];
@@ -331,7 +333,11 @@ __global__ void __launch_bounds__(kThreads, 4) index_select_kernel(const SelectA
   const uint4* kv = reinterpret_cast<const uint4*>(s_key);   // 16-byte reads of the keys
   const int nvec = key_words(rows_total) / 4;
   if (tid == 0) sm.gcount = 0u;
-  if (tid < kMaxCluster) sm.above_r[tid] = 0u;
+  if (tid < kMaxCluster) {
+    sm.above_r[tid] = 0u;
+    sm.gt_g[tid] = 0u;
+    sm.eq_g[tid] = 0u;
+  }
 
   // Selected: every key > T, plus the first q keys == T in index order.
   uint32_t T = 0u, q = 0u;
@@ -565,116 +571,170 @@ __global__ void __launch_bounds__(kThreads, 4) index_select_kernel(const SelectA
     }
     cluster_sync_all();   // the last remote access of the kernel
 
-    // every CTA finishes the selection alone over the G gathered words (0 = padding)
-    uint4* hl = reinterpret_cast<uint4*>(histL);
-    bool done = false;
-    Binning lflt{};                // after the first pass: the members are also in bin lsel of lflt
-    uint32_t lsel = 0u;
-    bool lf = false;
-    for (int it = 0; it < 12; ++it) {
-      uint32_t mn = 0xffffffffu, mx = 0u, c = 0u;
-      for (int i = tid; i < int(G); i += kThreads) {
-        const uint32_t kk = gk[i];
-        if (kk >= lo && kk <= hi && (!lf || bin_of(kk, lflt) == lsel)) {
-          mn = min(mn, kk);
-          mx = max(mx, kk);
-          ++c;
-        }
-      }
-      for (int j = tid; j < kBins * kCopiesL / 4; j += kThreads) hl[j] = make_uint4(0u, 0u, 0u, 0u);
-      mn = __reduce_min_sync(0xffffffffu, mn);
-      mx = __reduce_max_sync(0xffffffffu, mx);
-      c = __reduce_add_sync(0xffffffffu, c);
-      if (lane == 0) {
-        sm.red[0][warp] = c;
-        sm.red[1][warp] = mn;
-        sm.red[2][warp] = mx;
-      }
-      __syncthreads();
-      c = 0u;
-      mn = 0xffffffffu;
-      mx = 0u;
-      for (int w = 0; w < kWarpsAll; ++w) {
-        c += sm.red[0][w];
-        mn = min(mn, sm.red[1][w]);
-        mx = max(mx, sm.red[2][w]);
-      }
-      lo = mn;   // the members are now exactly the keys in [lo, hi]
-      hi = mx;
-      if (c == need) {
-        T = lo - 1u;
-        q = 0u;
-        done = true;
-        break;
-      }
-      if (lo == hi) {
-        T = lo;
-        q = need;
-        done = true;
-        break;
-      }
-      const Binning bl = make_binning(lo, hi, it < 2);
-      for (int i = tid; i < int(G); i += kThreads) {
-        const uint32_t kk = gk[i];
-        if (kk != 0u && kk >= lo && kk <= hi)
-          atomicAdd(&histL[bin_of(kk, bl) * kCopiesL + (lane & (kCopiesL - 1))], 1u);
-      }
-      __syncthreads();
-      for (int bin = tid; bin < kBins; bin += kThreads) {
-        const uint4 x = *reinterpret_cast<const uint4*>(&histL[bin * kCopiesL]);
-        const uint4 y = *reinterpret_cast<const uint4*>(&histL[bin * kCopiesL + 4]);
-        totL[bin] = x.x + x.y + x.z + x.w + y.x + y.y + y.z + y.w;
-      }
-      __syncthreads();
-      if (warp == 0) {
-        uint32_t g[8], local = 0u;
+    // Every CTA finishes the selection alone over the G gathered words: exactly
+    // the keys of the chosen bin, with zeros padding each CTA's segment to 4.
+    if (G <= uint32_t(2 * kThreads)) {
+      // Rank finish: the threshold T is the need-th largest gathered key, found
+      // by counting for each key the keys above and equal to it.
+      uint32_t x[2];
+      bool have[2];
 #pragma unroll
-        for (int j = 0; j < 8; ++j) {
-          g[j] = totL[kBins - 1 - lane * 8 - j];
-          local += g[j];
-        }
-        uint32_t incl = local;
+      for (int h = 0; h < 2; ++h) {
+        const int i = tid + h * kThreads;
+        x[h] = i < int(G) ? gk[i] : 0u;
+        have[h] = x[h] != 0u;
+      }
+      if (__any_sync(0xffffffffu, have[0] || have[1])) {
+        uint32_t cg[2] = {0u, 0u}, ce[2] = {0u, 0u};
+        const uint4* g4 = reinterpret_cast<const uint4*>(gk);
+        for (int i = 0; i < int(G >> 2); ++i) {   // the same address for every lane: a broadcast
+          const uint4 v = g4[i];
+          const uint32_t w[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
-        for (int o = 1; o < 32; o <<= 1) {
-          const uint32_t y = __shfl_up_sync(0xffffffffu, incl, o);
-          if (lane >= o) incl += y;
-        }
-        uint32_t before = incl - local;
+          for (int c = 0; c < 4; ++c)
 #pragma unroll
-        for (int j = 0; j < 8; ++j) {
-          if (before < need && before + g[j] >= need) {
-            sm.sel_bin = uint32_t(kBins - 1 - lane * 8 - j);
-            sm.sel_above = before;
+            for (int h = 0; h < 2; ++h) {
+              cg[h] += w[c] > x[h] ? 1u : 0u;
+              ce[h] += w[c] == x[h] ? 1u : 0u;
+            }
+        }
+#pragma unroll
+        for (int h = 0; h < 2; ++h)
+          if (have[h] && cg[h] < need && need <= cg[h] + ce[h]) {   // every holder of T writes the same
+            sm.sel_bin = x[h];
+            sm.sel_above = need - cg[h];
           }
-          before += g[j];
-        }
       }
       __syncthreads();
-      need -= sm.sel_above;
-      lflt = bl;
-      lsel = sm.sel_bin;
-      lf = true;
-    }
-    if (!done) report(a.err, kErrBadCount, -3);   // cannot happen: every pass narrows the range
-    // per CTA: gathered keys above and at the threshold
-    uint32_t seg_off = 0u;
-    for (int r = 0; r < int(ncta); ++r) {
-      const uint32_t n = sm.cnt_r[r];
-      if (r % kWarpsAll == warp) {
-        uint32_t gtc = 0u, eqc = 0u;
-        for (uint32_t i = lane; i < n; i += 32) {
-          const uint32_t kk = gk[seg_off + i];
-          gtc += kk > T ? 1u : 0u;
-          eqc += kk == T ? 1u : 0u;
-        }
-        gtc = __reduce_add_sync(0xffffffffu, gtc);
-        eqc = __reduce_add_sync(0xffffffffu, eqc);
-        if (lane == 0) {
-          sm.gt_r[r] = sm.above_r[r] + gtc;
-          sm.eq_r[r] = q > 0u ? eqc : 0u;
-        }
+      T = sm.sel_bin;
+      q = sm.sel_above;
+      // each CTA's gathered keys above and at T
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        if (!have[h] || x[h] < T) continue;
+        const uint32_t i = uint32_t(tid + h * kThreads);
+        int r = 0;
+        for (uint32_t off = (sm.cnt_r[0] + 3u) & ~3u; r + 1 < int(ncta) && i >= off; off += (sm.cnt_r[r] + 3u) & ~3u)
+          ++r;
+        atomicAdd(x[h] > T ? &sm.gt_g[r] : &sm.eq_g[r], 1u);
       }
-      seg_off += (n + 3u) & ~3u;
+      __syncthreads();
+      if (tid < int(ncta)) {
+        sm.gt_r[tid] = sm.above_r[tid] + sm.gt_g[tid];
+        sm.eq_r[tid] = sm.eq_g[tid];
+      }
+    } else {
+      // every CTA finishes the selection alone over the G gathered words (0 = padding)
+      uint4* hl = reinterpret_cast<uint4*>(histL);
+      bool done = false;
+      Binning lflt{};                // after the first pass: the members are also in bin lsel of lflt
+      uint32_t lsel = 0u;
+      bool lf = false;
+      for (int it = 0; it < 12; ++it) {
+        uint32_t mn = 0xffffffffu, mx = 0u, c = 0u;
+        for (int i = tid; i < int(G); i += kThreads) {
+          const uint32_t kk = gk[i];
+          if (kk >= lo && kk <= hi && (!lf || bin_of(kk, lflt) == lsel)) {
+            mn = min(mn, kk);
+            mx = max(mx, kk);
+            ++c;
+          }
+        }
+        for (int j = tid; j < kBins * kCopiesL / 4; j += kThreads) hl[j] = make_uint4(0u, 0u, 0u, 0u);
+        mn = __reduce_min_sync(0xffffffffu, mn);
+        mx = __reduce_max_sync(0xffffffffu, mx);
+        c = __reduce_add_sync(0xffffffffu, c);
+        if (lane == 0) {
+          sm.red[0][warp] = c;
+          sm.red[1][warp] = mn;
+          sm.red[2][warp] = mx;
+        }
+        __syncthreads();
+        c = 0u;
+        mn = 0xffffffffu;
+        mx = 0u;
+        for (int w = 0; w < kWarpsAll; ++w) {
+          c += sm.red[0][w];
+          mn = min(mn, sm.red[1][w]);
+          mx = max(mx, sm.red[2][w]);
+        }
+        lo = mn;   // the members are now exactly the keys in [lo, hi]
+        hi = mx;
+        if (c == need) {
+          T = lo - 1u;
+          q = 0u;
+          done = true;
+          break;
+        }
+        if (lo == hi) {
+          T = lo;
+          q = need;
+          done = true;
+          break;
+        }
+        const Binning bl = make_binning(lo, hi, it < 2);
+        for (int i = tid; i < int(G); i += kThreads) {
+          const uint32_t kk = gk[i];
+          if (kk != 0u && kk >= lo && kk <= hi)
+            atomicAdd(&histL[bin_of(kk, bl) * kCopiesL + (lane & (kCopiesL - 1))], 1u);
+        }
+        __syncthreads();
+        for (int bin = tid; bin < kBins; bin += kThreads) {
+          const uint4 x = *reinterpret_cast<const uint4*>(&histL[bin * kCopiesL]);
+          const uint4 y = *reinterpret_cast<const uint4*>(&histL[bin * kCopiesL + 4]);
+          totL[bin] = x.x + x.y + x.z + x.w + y.x + y.y + y.z + y.w;
+        }
+        __syncthreads();
+        if (warp == 0) {
+          uint32_t g[8], local = 0u;
+  #pragma unroll
+          for (int j = 0; j < 8; ++j) {
+            g[j] = totL[kBins - 1 - lane * 8 - j];
+            local += g[j];
+          }
+          uint32_t incl = local;
+  #pragma unroll
+          for (int o = 1; o < 32; o <<= 1) {
+            const uint32_t y = __shfl_up_sync(0xffffffffu, incl, o);
+            if (lane >= o) incl += y;
+          }
+          uint32_t before = incl - local;
+  #pragma unroll
+          for (int j = 0; j < 8; ++j) {
+            if (before < need && before + g[j] >= need) {
+              sm.sel_bin = uint32_t(kBins - 1 - lane * 8 - j);
+              sm.sel_above = before;
+            }
+            before += g[j];
+          }
+        }
+        __syncthreads();
+        need -= sm.sel_above;
+        lflt = bl;
+        lsel = sm.sel_bin;
+        lf = true;
+      }
+      if (!done) report(a.err, kErrBadCount, -3);   // cannot happen: every pass narrows the range
+      // per CTA: gathered keys above and at the threshold
+      uint32_t seg_off = 0u;
+      for (int r = 0; r < int(ncta); ++r) {
+        const uint32_t n = sm.cnt_r[r];
+        if (r % kWarpsAll == warp) {
+          uint32_t gtc = 0u, eqc = 0u;
+          for (uint32_t i = lane; i < n; i += 32) {
+            const uint32_t kk = gk[seg_off + i];
+            gtc += kk > T ? 1u : 0u;
+            eqc += kk == T ? 1u : 0u;
+          }
+          gtc = __reduce_add_sync(0xffffffffu, gtc);
+          eqc = __reduce_add_sync(0xffffffffu, eqc);
+          if (lane == 0) {
+            sm.gt_r[r] = sm.above_r[r] + gtc;
+            sm.eq_r[r] = q > 0u ? eqc : 0u;
+          }
+        }
+        seg_off += (n + 3u) & ~3u;
+      }
     }
   }
   __syncthreads();

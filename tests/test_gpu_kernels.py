@@ -309,6 +309,40 @@ def test_index_topk_fused(csa2, mode):
     assert_no_device_error(csa2, ws)
 
 
+@pytest.mark.parametrize("spread", [2, 1])
+def test_index_topk_fused_large_threshold_bin(csa2, spread):
+    """Fused flat scoring + Top-k when the bin holding the k-th score gathers about a
+    thousand keys (more than the rank-count finish takes), so the radix passes over
+    the gathered keys run: one-hot queries make every score 8 * k_idx[:, 0], with 100
+    rows at 2,560, 1,000 rows at 1,000 or 1,008 (one bin), the rest at 0."""
+    rng = np.random.default_rng(41)
+    B, N, K = 2, 4096, 256
+    sh = _shape(batch=B, n_entries=N, topk=K, pool_blocks=0)
+    col0 = np.zeros((B, N), dtype=np.float32)
+    for b in range(B):
+        rows = rng.permutation(N)
+        col0[b, rows[:100]] = 320.0
+        col0[b, rows[100:1100]] = 125.0 + rng.integers(0, spread, size=1000)
+    k_f = np.zeros((B, N, sh.idx_dim), dtype=np.float32)
+    k_f[:, :, 0] = col0
+    k_f[:, :, 1:] = rng.integers(-4, 5, size=(B, N, sh.idx_dim - 1))   # ignored by the one-hot queries
+    k_idx = W.f32_to_bf16_bits(k_f)
+    q_f = np.zeros((B, sh.idx_heads, sh.idx_dim), dtype=np.float32)
+    q_f[:, :, 0] = 1.0
+    q_idx = W.f32_to_bf16_bits(q_f)
+    w = np.ones((B, sh.idx_heads), dtype=np.float32)
+    n_valid = np.array([N, N - 3], dtype=np.int32)
+    ws = csa2.workspace(sh)
+    idx = torch.full((B, K), -9, dtype=torch.int32, device="cuda")
+    csa2.index_topk(sh, bf16(q_idx), f32(w), bf16(k_idx), i32(n_valid), K, idx, ws)
+    got = idx.cpu().numpy()
+    for b in range(B):
+        r = oracle.layer_indices(oracle.to_f64(q_idx[b]), w[b].astype(np.float64), oracle.to_f64(k_idx[b]), None,
+                                 int(n_valid[b]), topk=K, block=8, pool=0, hier=False)
+        assert got[b].tolist() == r["idx"].tolist(), f"spread {spread} query {b}"
+    assert_no_device_error(csa2, ws)
+
+
 @pytest.mark.parametrize("case", ["outlier", "relu_off"])
 def test_index_topk_pooled_wide_or_negative_scores(csa2, case):
     """Pooled scoring + Top-k when the 256 fixed bins below the top score hold fewer than
