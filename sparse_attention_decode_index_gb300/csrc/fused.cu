@@ -561,8 +561,8 @@ __global__ void __launch_bounds__(kThreads, 4) index_select_kernel(const SelectA
     if (tid < 3 && my_in + uint32_t(tid) < ((my_in + 3u) & ~3u)) gk[my_off + my_in + tid] = 0u;
     __syncthreads();
     {
-      const int nvec = int((my_in + 3u) >> 2);
-      for (int i = tid; i < nvec; i += kThreads) {
+      const int nseg = int((my_in + 3u) >> 2);   // 16-byte pieces of this CTA's segment
+      for (int i = tid; i < nseg; i += kThreads) {
         const uint32_t* src = gk + my_off + 4 * i;
         const uint4 v = *reinterpret_cast<const uint4*>(src);
         for (int r = 0; r < int(ncta); ++r)
