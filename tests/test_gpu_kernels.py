@@ -309,12 +309,13 @@ def test_index_topk_fused(csa2, mode):
     assert_no_device_error(csa2, ws)
 
 
-@pytest.mark.parametrize("spread", [2, 1])
-def test_index_topk_fused_large_threshold_bin(csa2, spread):
-    """Fused flat scoring + Top-k when the bin holding the k-th score gathers about a
-    thousand keys (more than the rank-count finish takes), so the radix passes over
-    the gathered keys run: one-hot queries make every score 8 * k_idx[:, 0], with 100
-    rows at 2,560, 1,000 rows at 1,000 or 1,008 (one bin), the rest at 0."""
+@pytest.mark.parametrize("group,spread", [(1000, 2), (1000, 1), (340, 1), (280, 1), (280, 2)])
+def test_index_topk_fused_large_threshold_bin(csa2, group, spread):
+    """Fused flat scoring + Top-k when the bin holding the k-th score gathers `group`
+    keys: one-hot queries make every score 8 * k_idx[:, 0], with 100 rows at 2,560,
+    `group` rows at 1,000 or 1,008 (one bin; all 1,000 when spread is 1, a tie across
+    the CTAs), the rest at 0.  1,000 and 340 gathered keys take the radix passes over
+    the gathered keys; 280 (at most 304 words with padding) take the rank-count finish."""
     rng = np.random.default_rng(41)
     B, N, K = 2, 4096, 256
     sh = _shape(batch=B, n_entries=N, topk=K, pool_blocks=0)
@@ -322,7 +323,7 @@ def test_index_topk_fused_large_threshold_bin(csa2, spread):
     for b in range(B):
         rows = rng.permutation(N)
         col0[b, rows[:100]] = 320.0
-        col0[b, rows[100:1100]] = 125.0 + rng.integers(0, spread, size=1000)
+        col0[b, rows[100:100 + group]] = 125.0 + rng.integers(0, spread, size=group)
     k_f = np.zeros((B, N, sh.idx_dim), dtype=np.float32)
     k_f[:, :, 0] = col0
     k_f[:, :, 1:] = rng.integers(-4, 5, size=(B, N, sh.idx_dim - 1))   # ignored by the one-hot queries
@@ -339,7 +340,7 @@ def test_index_topk_fused_large_threshold_bin(csa2, spread):
     for b in range(B):
         r = oracle.layer_indices(oracle.to_f64(q_idx[b]), w[b].astype(np.float64), oracle.to_f64(k_idx[b]), None,
                                  int(n_valid[b]), topk=K, block=8, pool=0, hier=False)
-        assert got[b].tolist() == r["idx"].tolist(), f"spread {spread} query {b}"
+        assert got[b].tolist() == r["idx"].tolist(), f"group {group} spread {spread} query {b}"
     assert_no_device_error(csa2, ws)
 
 
