@@ -337,6 +337,21 @@ __global__ void __launch_bounds__(kThreads, 2) attn_mma_kernel(const AttnArgs a)
         }
       *reinterpret_cast<float4*>(a.out + ((long long)b * kH + h) * kDv + 4 * d4) = acc;
     }
+    // The partials just combined are dead (every launch writes them before it
+    // reads them): drop their L2 lines instead of letting them be written back
+    // to HBM during the next launches' streams.  The 8 lanes 8g .. 8g + 7 read
+    // one 128-byte line of each CTA's partial row; lane 8g + r drops CTA r's.
+    __syncwarp();
+#pragma unroll
+    for (int m = 0; m < kItems; ++m) {
+      const int e = e0 + m * kThreads;
+      const int r = lane & 7;
+      if (e < n_items && r < int(ncta)) {
+        const int h = hb + e / (kDv / 4), d4 = (e % (kDv / 4)) & ~7;
+        const float* line = a.part + ((size_t)(b * int(ncta) + r) * kH + h) * kDv + 4 * d4;
+        asm volatile("discard.global.L2 [%0], 128;" ::"l"(line) : "memory");
+      }
+    }
   }
   if (a.lse != nullptr && tid < he - hb) {
     const int h = hb + tid;
