@@ -625,10 +625,10 @@ def end_to_end(csa2, wl, d, graph, stream, flush, args, dev):
     torch.cuda.synchronize()
     for i in range(n):
         s_ = i % 2
-        if i == args.warmup:
-            t0.record(up)
         if i >= 2:
             up.wait_event(ev_comp[i - 2])          # set s_'s inputs were read by step i-2
+        if i == args.warmup:
+            t0.record(up)                          # the first timed step's input copy starts here
         with torch.cuda.stream(up):
             g_in[s_].replay()
         ev_in[i].record(up)
@@ -649,7 +649,8 @@ def end_to_end(csa2, wl, d, graph, stream, flush, args, dev):
     return {"value": sh.batch * world * args.steps / total, "unit": UNIT, "h2d_bytes_per_step": h2d,
             "d2h_bytes_per_step": d2h, "ms_per_step": 1e3 * total / args.steps,
             "pipeline": "inputs of step i+1 copied in and outputs of step i copied out while step i computes; "
-                        "two buffer sets; steps serialised on the compute stream",
+                        "two buffer sets; steps serialised on the compute stream; timed from the start of the "
+                        "first timed step's input copy to the end of the last timed step's output copy",
             "l2": f"not flushed between steps: each step reads {algorithmic_bytes(wl)['total'] / 1e6:.0f} MB of "
                   "algorithmic bytes" + (", more than the 129 MB L2" if algorithmic_bytes(wl)["total"] > 129e6
                                          else " (fits in L2: later steps may hit it)"),
