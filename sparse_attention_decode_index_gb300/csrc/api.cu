@@ -226,8 +226,9 @@ int do_topk(const csa2_shape& s, const WsLayout& L, void* ws, const float* score
 
 int do_attn(const csa2_shape& s, const void* q, const void* k_main, const void* v_main, const int32_t* idx,
             const void* k_swa, const void* v_swa, const int32_t* n_swa, float* out, float* lse, int* err,
-            float* part, cudaStream_t st, bool swa_only = false) {
+            float* part, cudaStream_t st, bool swa_only = false, bool release_at_end = false) {
   AttnArgs a{};
+  a.release_at_end = release_at_end ? 1 : 0;
   a.q = q;
   a.k_main = k_main;
   a.v_main = v_main;
@@ -547,9 +548,11 @@ int csa2_layer_group(const csa2_shape* shape, const csa2_layer* layers, int32_t 
   const int32_t* cur = nullptr;
   for (int l = 0; l < n_layers; ++l) {
     const csa2_layer& y = layers[l];
+    // another attention-only launch next (Reuse or SWA layer): release it at this attention's end
+    const bool attn_next = l + 1 < n_layers && (layers[l + 1].mode == CSA2_REUSE || layers[l + 1].mode == CSA2_SWA);
     if (y.mode == CSA2_SWA) {
       CSA2_TRY(do_attn(s, y.q, k_main, v_main, nullptr, y.k_swa, y.v_swa, n_swa, y.out, y.lse, err,
-                     at<float>(ws, L.attn_part), stream, true));
+                     at<float>(ws, L.attn_part), stream, true, attn_next));
       continue;
     }
     if (y.mode != CSA2_REUSE) {
@@ -588,7 +591,7 @@ int csa2_layer_group(const csa2_shape* shape, const csa2_layer* layers, int32_t 
       cur = dst;
     }
     CSA2_TRY(do_attn(s, y.q, k_main, v_main, cur, y.k_swa, y.v_swa, n_swa, y.out, y.lse, err,
-                     at<float>(ws, L.attn_part), stream));
+                     at<float>(ws, L.attn_part), stream, false, attn_next));
   }
   return CSA2_OK;
 }

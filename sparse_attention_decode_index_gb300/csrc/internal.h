@@ -68,6 +68,7 @@ struct AttnArgs {
   float scale;               // softmax scale (natural-log domain)
   float* part;               // fast path: [B, cluster, H, dv] fp32 partials (workspace scratch)
   int* err;
+  int release_at_end;        // fast path: let the next launch place its CTAs only at this one's end
 };
 
 // Fused scoring + cluster Top-k (fused.cu): one cluster per query scores its
