@@ -28,8 +28,9 @@
 // CTA pushes its per-head (m, l) into the table of the CTA that owns those
 // heads (distributed shared memory) and writes its unscaled partial O, as
 // 16-byte vectors assembled from lane pairs, to workspace scratch that stays
-// in L2; the owner then weights the partials by exp2(m_c - M) / L and sums them
-// in fixed CTA order, so the result is deterministic.  (Pushing the partials
+// in L2; the owner then weights the partials by exp2(m_c - M) / L, sums them
+// in fixed CTA order, so the result is deterministic, and drops their L2 lines
+// (discard, no write-back: every launch rewrites them).  (Pushing the partials
 // through distributed shared memory instead needs a second barrier -- they
 // would land in the K region while a peer may still be reading it -- and was
 // measured slower.)
