@@ -39,6 +39,7 @@ if ROOT not in sys.path:
 from sparse_attention_decode_index_gb300 import workloads as W  # noqa: E402
 
 METRIC = "CSA2 decode queries/sec per layer group at 128K ctx; % of GB300 HBM roofline"
+FUSED_MAX_ROWS = 32768          # rows per query served by the fused flat scoring + Top-K (8 CTAs x 4,096)
 UNIT = "queries/s"
 L2_BYTES = 129 * 1024 * 1024
 
@@ -185,11 +186,15 @@ def _oracle_worker(conn):
 
 
 def slice_queries(wl, queries):
-    """A workload holding only the given queries of ``wl`` (batch = len(queries))."""
+    """A workload holding only the given queries of ``wl`` (batch = len(queries), one token per
+    sequence: with ``shape.tokens`` = T > 1 query q reads cache sequence q // T, whose caches the
+    slice copies)."""
     import copy
+    T = max(1, int(getattr(wl.shape, "tokens", 1)))
+    seqs = [q // T for q in queries]
     sub = copy.copy(wl)
-    sub.shape = W.Shape(**{**wl.shape.__dict__, "batch": len(queries)})
-    sub.k_main, sub.v_main, sub.k_idx = wl.k_main[queries], wl.v_main[queries], wl.k_idx[queries]
+    sub.shape = W.Shape(**{**wl.shape.__dict__, "batch": len(queries), "tokens": 1})
+    sub.k_main, sub.v_main, sub.k_idx = wl.k_main[seqs], wl.v_main[seqs], wl.k_idx[seqs]
     sub.n_valid, sub.n_swa = wl.n_valid[queries], wl.n_swa[queries]
     sub.layers = [W.Layer(mode=L.mode, hier=L.hier, q=L.q[queries], k_swa=L.k_swa[queries],
                           v_swa=L.v_swa[queries], q_idx=None if L.q_idx is None else L.q_idx[queries],
@@ -249,18 +254,21 @@ class OraclePool:
             p.join(timeout=10)
 
 
-def cpu_baseline(wl, min_seconds: float = 10.0, max_steps: int = 20) -> dict:
-    pool = OraclePool(wl)
+CPU_SAMPLE_SECONDS = 10.0       # wall time of the oracle sample (bounded: at most CPU_SAMPLE_PASSES passes)
+CPU_SAMPLE_PASSES = 2000
+
+
+def cpu_sample(pool, wl) -> dict:
+    """Time the oracle pool on repeated passes over its sample for about CPU_SAMPLE_SECONDS."""
     try:
         times = [pool.step()]
-        while sum(times) < min_seconds and len(times) < max_steps:
+        while sum(times) < CPU_SAMPLE_SECONDS and len(times) < CPU_SAMPLE_PASSES:
             times.append(pool.step())
     finally:
         pool.close()
-    q = pool.queries * len(times)
-    return {"value": q / sum(times), "unit": UNIT, "cores": pool.workers, "kind": "oracle",
-            "sample": f"{pool.queries} of the {wl.shape.batch} queries of {wl.name} (one per worker process), "
-                      f"{len(times)} passes, {sum(times):.1f} s wall"}
+    return {"value": pool.queries * len(times) / sum(times), "unit": UNIT, "cores": pool.workers, "kind": "oracle",
+            "sample": f"{pool.queries} of the {wl.shape.batch} queries of {wl.name} (one per worker process, 1 BLAS "
+                      f"thread each), {len(times)} passes, {sum(times):.1f} s wall"}
 
 
 def run_reference(args):
@@ -400,18 +408,7 @@ def run_ours(args):
     clocks["window"] = (f"nvidia-smi every 200 ms over the timed steps plus {args.clock_soak:.1f} s before and "
                         f"{args.clock_soak / 2:.1f} s after of untimed replays of the same step")
 
-    cpu = None
-    if pool is not None:
-        try:
-            times = [pool.step()]
-            while sum(times) < 10.0 and len(times) < 20:
-                times.append(pool.step())
-        finally:
-            pool.close()
-        cpu = {"value": pool.queries * len(times) / sum(times), "unit": UNIT, "cores": pool.workers,
-               "kind": "oracle",
-               "sample": f"{pool.queries} of the {sh.batch} queries of {wl.name} (one per worker process, 1 BLAS "
-                         f"thread each), {len(times)} passes, {sum(times):.1f} s wall"}
+    cpu = cpu_sample(pool, wl) if pool is not None else None
     if rank == 0:
         line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
                 "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
@@ -431,29 +428,32 @@ def run_ours(args):
     return 0
 
 
-def profiled_traffic(wl, hier: bool):
-    """DRAM bytes per launch of the fused pooled kernel from the committed ncu summary, or None
-    when no summary covers this workload or the kernel source changed since it was captured."""
+KERNEL_SOURCES = ("fused.cu", "common.cuh", "internal.h")
+
+
+def kernel_source_hash() -> str:
+    """First 16 hex digits of the SHA-256 of the fused selection kernel's sources."""
     import hashlib
-    if not hier or wl.name != "reindex_b64_128k":
-        return None, "no ncu capture of this workload's kernel"
-    prof = os.path.join(ROOT, "profiles", "index_select_pooled__reindex_b64_128k.md")
-    if not os.path.exists(prof):
-        return None, "no ncu summary"
-    fields = {}
-    with open(prof) as f:
-        for line in f:
-            if ":" in line and line.split(":")[0].strip() in ("dram_bytes_per_launch", "source_sha256_16"):
-                k, v = line.split(":", 1)
-                fields[k.strip()] = v.strip()
     h = hashlib.sha256()
-    for name in ("fused.cu", "common.cuh", "internal.h"):
+    for name in KERNEL_SOURCES:
         with open(os.path.join(ROOT, "sparse_attention_decode_index_gb300", "csrc", name), "rb") as f:
             h.update(f.read())
-    if fields.get("source_sha256_16") != h.hexdigest()[:16]:
+    return h.hexdigest()[:16]
+
+
+def profiled_traffic(wl, hier: bool):
+    """DRAM bytes per launch of the dominant kernel from the committed ncu capture
+    (profiles/<kernel>__<workload>.traffic.json, written beside its summary), or None when no
+    capture covers this workload or the kernel's source changed since it was captured."""
+    name = f"index_select_{'pooled' if hier else 'flat'}__{wl.name}.traffic.json"
+    path = os.path.join(ROOT, "profiles", name)
+    if not os.path.exists(path):
+        return None, "no ncu capture of this workload's dominant kernel"
+    with open(path) as f:
+        rec = json.load(f)
+    if rec.get("source_sha256_16") != kernel_source_hash():
         return None, "kernel source changed since the ncu capture"
-    return int(fields["dram_bytes_per_launch"]), "dram__bytes_read.sum + dram__bytes_write.sum, " + \
-        "profiles/index_select_pooled__reindex_b64_128k.md"
+    return int(rec["dram_bytes_per_launch"]), "dram__bytes_read.sum + dram__bytes_write.sum, profiles/" + name
 
 
 def dominant_kernel_roofline(csa2, wl, d, stream, flush, args, peak, peak_src):
@@ -465,6 +465,7 @@ def dominant_kernel_roofline(csa2, wl, d, stream, flush, args, peak, peak_src):
     dev = d["k_idx"].device
     reps = max(args.steps, 10)
     idx = torch.empty((sh.batch, sh.topk), dtype=torch.int32, device=dev)
+    fused_flat = sh.n_entries <= FUSED_MAX_ROWS
     with torch.cuda.stream(stream):
         if hier:
             pool = torch.empty((sh.batch, sh.pool_blocks), dtype=torch.int32, device=dev)
@@ -477,11 +478,20 @@ def dominant_kernel_roofline(csa2, wl, d, stream, flush, args, peak, peak_src):
             name = ("index_select_kernel<pooled> (csa2_index_topk: pooled token scoring + exact Top-512, "
                     "one cluster per query)")
             n_rows = sum(min(sh.pool_blocks, -(-int(v) // sh.block)) * sh.block for v in wl.n_valid)
-        else:
+        elif fused_flat:
             def launch():
                 csa2.index_topk(sh, L0["q_idx"], L0["w_idx"], d["k_idx"], d["n_valid"], sh.topk, idx, d["ws"],
                                 stream=stream)
             name = "index_select_kernel<flat> (csa2_index_topk: flat token scoring + exact Top-512)"
+            n_rows = int(sum(int(v) for v in wl.n_valid))
+        else:
+            scores = torch.empty((sh.batch, sh.n_entries), dtype=torch.float32, device=dev)
+
+            def launch():
+                csa2.index_tokens(sh, L0["q_idx"], L0["w_idx"], d["k_idx"], d["n_valid"], scores, d["ws"],
+                                  stream=stream)
+            name = ("indexer_mma_kernel<flat> (csa2_index_tokens: flat token scoring of the Full layer, "
+                    "scores written to HBM)")
             n_rows = int(sum(int(v) for v in wl.n_valid))
         launch()
         torch.cuda.synchronize()
@@ -496,6 +506,8 @@ def dominant_kernel_roofline(csa2, wl, d, stream, flush, args, peak, peak_src):
             ms.append(e0.elapsed_time(e1))
     e = 4 if sh.dtype == "f32" else 2
     alg = n_rows * sh.idx_dim * e
+    if not hier and not fused_flat:
+        alg += n_rows * 4                                 # the fp32 score of every row is written
     avg = sum(ms) / len(ms)
     gbs = alg / (avg / 1e3) / 1e9
     traffic, traffic_src = profiled_traffic(wl, hier)

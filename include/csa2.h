@@ -27,7 +27,8 @@
  *     (keys, main KV, SWA KV, queries) must be 16-byte aligned.
  *   - Work is enqueued on `stream` (a cudaStream_t; NULL = legacy default
  *     stream).  No entry point allocates or frees memory, and none
- *     synchronises except csa2_read_device_error.
+ *     synchronises except csa2_read_device_error and
+ *     csa2_read_static_device_error.
  *   - Arguments are validated on the host before anything is enqueued; a
  *     negative csa2_status is returned and nothing is launched.  A failed
  *     launch returns CSA2_ERR_CUDA.
@@ -47,7 +48,12 @@
  *   - `ws` is a caller-owned device workspace of at least
  *     csa2_workspace_bytes(shape) bytes, 256-byte aligned, zeroed once with
  *     csa2_workspace_init before first use.  Calls that share a workspace
- *     must be ordered on one stream.
+ *     must be ordered on one stream.  The cache-maintenance calls
+ *     (csa2_block_keys, csa2_kv_append, csa2_swa_append) use only the
+ *     workspace's error word; they also accept ws = NULL with ws_bytes = 0,
+ *     and then record device errors in the header of the library's static
+ *     scratch array (see csa2_layer_group_static), where
+ *     csa2_read_static_device_error reads them.
  *   - Element type (csa2_shape.dtype): bf16 or fp32, for queries, keys,
  *     values and indexer tensors alike.  Scores, weights, outputs and lse are
  *     fp32; indices and counts are int32.
@@ -273,20 +279,30 @@ int csa2_layer_group(const csa2_shape* shape, const csa2_layer* layers, int32_t 
  * This entry point takes the same arguments as csa2_layer_group minus the
  * workspace, and runs the same layer group on a 32 MiB scratch array that the
  * library holds in device memory (a file-scope __device__ array: every GPU
- * that loads the library keeps it until the process exits).
+ * that loads the library keeps it until the process exits; it starts zeroed).
  *   - Shapes whose csa2_workspace_bytes exceeds 32 MiB return
  *     CSA2_ERR_WORKSPACE and enqueue nothing.
  *   - The first call made while a device is current looks up the array's
- *     device address and zeroes its header (the sticky device error word) on
- *     `stream`; make that first call before any stream capture.
+ *     device address (once per device, safe against host threads making
+ *     their first calls at the same time); make that first call before any
+ *     stream capture.
  *   - Every call shares the one array: calls that may overlap on the GPU (on
  *     different streams, or from different host threads without ordering)
  *     race on it and must be serialised by the caller.
- *   - No memory is allocated or freed; device-side range problems are still
- *     skipped by the kernels as in csa2_layer_group. */
+ *   - No memory is allocated or freed.  Device-side range problems are
+ *     skipped by the kernels as in csa2_layer_group and recorded in the
+ *     array's header; read them with csa2_read_static_device_error.
+ *   - kb can be prepared without a workspace too: csa2_block_keys and
+ *     csa2_kv_append accept ws = NULL, ws_bytes = 0. */
 int csa2_layer_group_static(const csa2_shape* shape, const csa2_layer* layers, int32_t n_layers,
                             const void* k_main, const void* v_main, const void* k_idx, const void* kb,
                             const int32_t* n_valid, const int32_t* n_swa, csa2_stream_t stream);
+
+/* csa2_read_device_error for the static scratch array of the current device
+ * (the error word of csa2_layer_group_static and of cache-maintenance calls
+ * made with ws = NULL): synchronises `stream`, returns and clears the word.
+ * The paper has no counterpart. */
+int csa2_read_static_device_error(csa2_stream_t stream, int32_t* detail);
 
 /* Static description of a status code. */
 const char* csa2_status_str(int status);
@@ -305,6 +321,21 @@ int csa2_fast_path(const csa2_shape* shape, int32_t* indexer_fast, int32_t* atte
  * (all threads and devices; launches recorded into a CUDA graph count once,
  * at capture).  For diagnostics and launch accounting. */
 unsigned long long csa2_launch_count(void);
+
+/* Test hook of the device-side failure detection (diagnostics; the paper has
+ * no counterpart).  Runs the fused flat scoring + Top-k of csa2_index_topk
+ * (pool == NULL; fast path only, else CSA2_ERR_UNSUPPORTED) with the copy of
+ * every CTA's first key tile left out, so that the tile's stage barrier can
+ * never complete, and with every bounded wait limited to wait_limit_ns
+ * (1,000 .. 100,000,000) instead of 2 s.  The waits give up, the kernel
+ * records CSA2_ERR_TIMEOUT (bit 2) in the workspace's error word, the CTAs
+ * that gave up offer no candidate, and the kernel returns: no copy is in
+ * flight when a wait gives up and every write stays inside idx_out [B, k].
+ * csa2_read_device_error then returns CSA2_ERR_TIMEOUT, and the stream and
+ * context stay usable. */
+int csa2_debug_wait_timeout(const csa2_shape* shape, const void* q_idx, const float* w, const void* k_idx,
+                            const int32_t* n_valid, int32_t k, int32_t* idx_out, uint32_t wait_limit_ns,
+                            void* ws, size_t ws_bytes, csa2_stream_t stream);
 
 #ifdef __cplusplus
 }

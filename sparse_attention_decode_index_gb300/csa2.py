@@ -71,6 +71,9 @@ _SIGS = {
     "csa2_launch_count": (ctypes.c_ulonglong, []),
     "csa2_layer_group_static": (ctypes.c_int, [ctypes.POINTER(CShape), ctypes.POINTER(CLayer), _I32, _VP, _VP,
                                                _VP, _VP, _VP, _VP, _VP]),
+    "csa2_read_static_device_error": (ctypes.c_int, [_VP, ctypes.POINTER(_I32)]),
+    "csa2_debug_wait_timeout": (ctypes.c_int, [ctypes.POINTER(CShape), _VP, _VP, _VP, _VP, _I32, _VP, ctypes.c_uint32,
+                                               _VP, _SZ, _VP]),
 }
 
 
@@ -137,6 +140,13 @@ def _stream(stream) -> Optional[int]:
     return getattr(stream, "cuda_stream", stream)
 
 
+def _ws(ws):
+    """(pointer, bytes) of a workspace; None passes no workspace (NULL, 0)."""
+    if ws is None:
+        return None, 0
+    return _ptr(ws, torch.uint8, "ws"), ws.numel()
+
+
 def _check(status: int, what: str):
     if status != OK:
         raise CSA2Error(status, what)
@@ -165,11 +175,13 @@ def workspace(shape, device=None, stream=None) -> torch.Tensor:
 
 
 def block_keys(shape, k_idx, n_valid, kb, ws, round_to_int: bool = True, stream=None):
+    """Block summary keys into kb.  ``ws`` may be None: device errors then go to the
+    static scratch's error word (read_static_device_error)."""
     s = c_shape(shape)
     e = elem_dtype(shape)
     _check(lib().csa2_block_keys(ctypes.byref(s), _ptr(k_idx, e, "k_idx"), _ptr(n_valid, torch.int32, "n_valid"),
-                                 int(bool(round_to_int)), _ptr(kb, e, "kb"), _ptr(ws, torch.uint8, "ws"),
-                                 ws.numel(), _stream(stream)), "csa2_block_keys")
+                                 int(bool(round_to_int)), _ptr(kb, e, "kb"), *_ws(ws), _stream(stream)),
+           "csa2_block_keys")
 
 
 def kv_append(shape, n_new, k_new, v_new, kidx_new, k_main, v_main, k_idx, kb, n_valid, ws,
@@ -182,8 +194,8 @@ def kv_append(shape, n_new, k_new, v_new, kidx_new, k_main, v_main, k_idx, kb, n
     _check(lib().csa2_kv_append(ctypes.byref(s), max_new, _ptr(n_new, torch.int32, "n_new"), _ptr(k_new, e, "k_new"),
                                 _ptr(v_new, e, "v_new"), _ptr(kidx_new, e, "kidx_new"), _ptr(k_main, e, "k_main"),
                                 _ptr(v_main, e, "v_main"), _ptr(k_idx, e, "k_idx"), _ptr(kb, e, "kb"),
-                                _ptr(n_valid, torch.int32, "n_valid"), int(bool(round_to_int)),
-                                _ptr(ws, torch.uint8, "ws"), ws.numel(), _stream(stream)), "csa2_kv_append")
+                                _ptr(n_valid, torch.int32, "n_valid"), int(bool(round_to_int)), *_ws(ws),
+                                _stream(stream)), "csa2_kv_append")
 
 
 class CSwaSlot(ctypes.Structure):
@@ -201,7 +213,7 @@ def swa_append(shape, slots, swa_head, n_swa, ws, stream=None):
                                              _ptr(vs, e, "v_swa")) for kt, vt, ks, vs in slots])
     _check(lib().csa2_swa_append(ctypes.byref(s), ctypes.cast(arr, ctypes.c_void_p), len(slots),
                                  _ptr(swa_head, torch.int32, "swa_head"), _ptr(n_swa, torch.int32, "n_swa"),
-                                 _ptr(ws, torch.uint8, "ws"), ws.numel(), _stream(stream)), "csa2_swa_append")
+                                 *_ws(ws), _stream(stream)), "csa2_swa_append")
 
 
 def index_blocks(shape, q_idx, w, kb, n_valid, pool_out, n_pool_out, ws, stream=None):
@@ -312,6 +324,26 @@ def read_device_error(ws, stream=None):
     d = _I32(0)
     st = lib().csa2_read_device_error(_ptr(ws, torch.uint8, "ws"), _stream(stream), ctypes.byref(d))
     return int(st), int(d.value)
+
+
+def read_static_device_error(stream=None):
+    """Synchronise and read/clear the error word of the library's static scratch on the
+    current device (csa2_layer_group_static, and cache-maintenance calls made with
+    ws=None): (status, detail bits)."""
+    d = _I32(0)
+    st = lib().csa2_read_static_device_error(_stream(stream), ctypes.byref(d))
+    return int(st), int(d.value)
+
+
+def debug_wait_timeout(shape, q_idx, w, k_idx, n_valid, k: int, idx_out, wait_limit_ns: int, ws, stream=None):
+    """Test hook of the bounded device waits (csa2_debug_wait_timeout): the fused flat selection
+    with every CTA's first tile left uncopied and waits limited to ``wait_limit_ns``."""
+    s = c_shape(shape)
+    e = elem_dtype(shape)
+    _check(lib().csa2_debug_wait_timeout(ctypes.byref(s), _ptr(q_idx, e, "q_idx"), _ptr(w, torch.float32, "w"),
+                                         _ptr(k_idx, e, "k_idx"), _ptr(n_valid, torch.int32, "n_valid"), int(k),
+                                         _ptr(idx_out, torch.int32, "idx_out"), int(wait_limit_ns),
+                                         *_ws(ws), _stream(stream)), "csa2_debug_wait_timeout")
 
 
 def launch_count() -> int:

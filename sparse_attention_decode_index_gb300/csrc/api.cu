@@ -9,6 +9,7 @@
 #include <atomic>
 #include <cstdint>
 #include <cstring>
+#include <mutex>
 
 #include "../../include/csa2.h"
 #include "internal.h"
@@ -18,6 +19,24 @@ using namespace csa2;
 namespace csa2 {
 static std::atomic<unsigned long long> g_launches{0};
 void note_launch() { g_launches.fetch_add(1, std::memory_order_relaxed); }
+
+constexpr int kMaxSetupDevices = 64;
+static std::atomic<uint64_t> g_setup_done[kMaxSetupDevices];
+static std::mutex g_setup_mu;
+
+cudaError_t once_per_device(int key, cudaError_t (*set)()) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= kMaxSetupDevices || key < 0 || key >= 64) return set();
+  const uint64_t bit = uint64_t(1) << key;
+  if (g_setup_done[dev].load(std::memory_order_acquire) & bit) return cudaSuccess;
+  std::lock_guard<std::mutex> lock(g_setup_mu);
+  if (g_setup_done[dev].load(std::memory_order_relaxed) & bit) return cudaSuccess;
+  e = set();
+  if (e == cudaSuccess) g_setup_done[dev].fetch_or(bit, std::memory_order_release);
+  return e;
+}
 }  // namespace csa2
 
 namespace {
@@ -78,6 +97,12 @@ T* at(void* ws, size_t off) {
   return reinterpret_cast<T*>(static_cast<uint8_t*>(ws) + off);
 }
 
+#define CSA2_TRY(x)                   \
+  do {                                \
+    const int _st = (x);              \
+    if (_st != CSA2_OK) return _st;   \
+  } while (0)
+
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
 int check_shape(const csa2_shape* s) {
@@ -115,13 +140,22 @@ int check_ws(const csa2_shape& s, void* ws, size_t bytes) {
 
 int cuda_status(cudaError_t e) { return e == cudaSuccess ? CSA2_OK : CSA2_ERR_CUDA; }
 
-float softmax_scale(const csa2_shape& s) { return s.scale > 0.f ? s.scale : 1.0f / sqrtf(float(s.k_dim)); }
+// Device error word of a cache-maintenance call: the header of the caller's
+// workspace, or, when the caller passes no workspace (ws NULL, ws_bytes 0),
+// the header of the library's static scratch array on the current device.
+int error_word(const csa2_shape& s, void* ws, size_t ws_bytes, int** err) {
+  if (ws == nullptr && ws_bytes == 0) {
+    void* p = nullptr;
+    CSA2_TRY(static_scratch(&p));
+    *err = static_cast<int*>(p);
+    return CSA2_OK;
+  }
+  CSA2_TRY(check_ws(s, ws, ws_bytes));
+  *err = static_cast<int*>(ws);
+  return CSA2_OK;
+}
 
-#define CSA2_TRY(x)                   \
-  do {                                \
-    const int _st = (x);              \
-    if (_st != CSA2_OK) return _st;   \
-  } while (0)
+float softmax_scale(const csa2_shape& s) { return s.scale > 0.f ? s.scale : 1.0f / sqrtf(float(s.k_dim)); }
 
 // ---------------------------------------------------------------- internal ops (no validation)
 
@@ -324,9 +358,10 @@ int csa2_block_keys(const csa2_shape* shape, const void* k_idx, const int32_t* n
                     void* kb, void* ws, size_t ws_bytes, csa2_stream_t stream) {
   CSA2_TRY(check_shape(shape));
   const csa2_shape& s = *shape;
-  CSA2_TRY(check_ws(s, ws, ws_bytes));
   if (k_idx == nullptr || n_valid == nullptr || kb == nullptr) return CSA2_ERR_INVALID_ARG;
   if (round_to_int != 0 && round_to_int != 1) return CSA2_ERR_INVALID_ARG;
+  int* err = nullptr;
+  CSA2_TRY(error_word(s, ws, ws_bytes, &err));
   const WsLayout L = layout(s);
   BlockKeyArgs a{};
   a.k_idx = k_idx;
@@ -339,7 +374,7 @@ int csa2_block_keys(const csa2_shape* shape, const void* k_idx, const int32_t* n
   a.block = s.block;
   a.round_to_int = round_to_int;
   a.dtype = s.dtype;
-  a.err = at<int>(ws, L.hdr);
+  a.err = err;
   return cuda_status(launch_block_keys(a, s.batch, stream));
 }
 
@@ -348,13 +383,14 @@ int csa2_kv_append(const csa2_shape* shape, int32_t max_new, const int32_t* n_ne
                    int32_t* n_valid, int32_t round_to_int, void* ws, size_t ws_bytes, csa2_stream_t stream) {
   CSA2_TRY(check_shape(shape));
   const csa2_shape& s = *shape;
-  CSA2_TRY(check_ws(s, ws, ws_bytes));
   if (seqdiv(s) != 1) return CSA2_ERR_UNSUPPORTED;   // appends are per sequence: pass a one-token shape
   if (max_new < 0 || max_new > s.n_entries) return CSA2_ERR_INVALID_ARG;
   if (n_new == nullptr || n_valid == nullptr || k_main == nullptr || v_main == nullptr || k_idx == nullptr)
     return CSA2_ERR_INVALID_ARG;
   if (max_new > 0 && (k_new == nullptr || v_new == nullptr || kidx_new == nullptr)) return CSA2_ERR_INVALID_ARG;
   if (round_to_int != 0 && round_to_int != 1) return CSA2_ERR_INVALID_ARG;
+  int* err = nullptr;
+  CSA2_TRY(error_word(s, ws, ws_bytes, &err));
   const WsLayout L = layout(s);
   KvAppendArgs a{};
   a.n_new = n_new;
@@ -375,7 +411,7 @@ int csa2_kv_append(const csa2_shape* shape, int32_t max_new, const int32_t* n_ne
   a.block = s.block;
   a.round_to_int = round_to_int;
   a.dtype = s.dtype;
-  a.err = at<int>(ws, L.hdr);
+  a.err = err;
   return cuda_status(launch_kv_append(a, s.batch, stream));
 }
 
@@ -383,11 +419,11 @@ int csa2_swa_append(const csa2_shape* shape, const csa2_swa_slot* layers, int32_
                     int32_t* n_swa, void* ws, size_t ws_bytes, csa2_stream_t stream) {
   CSA2_TRY(check_shape(shape));
   const csa2_shape& s = *shape;
-  CSA2_TRY(check_ws(s, ws, ws_bytes));
   if (seqdiv(s) != 1) return CSA2_ERR_UNSUPPORTED;   // rings are per query: pass a one-token shape
   if (s.swa < 1 || layers == nullptr || n_layers < 1 || n_layers > kMaxSwaLayers) return CSA2_ERR_INVALID_ARG;
   if (swa_head == nullptr || n_swa == nullptr) return CSA2_ERR_INVALID_ARG;
-  const WsLayout L = layout(s);
+  int* err = nullptr;
+  CSA2_TRY(error_word(s, ws, ws_bytes, &err));
   SwaAppendArgs a{};
   for (int l = 0; l < n_layers; ++l) {
     const csa2_swa_slot& y = layers[l];
@@ -402,7 +438,7 @@ int csa2_swa_append(const csa2_shape* shape, const csa2_swa_slot* layers, int32_
   a.k_dim = s.k_dim;
   a.v_dim = s.v_dim;
   a.dtype = s.dtype;
-  a.err = at<int>(ws, L.hdr);
+  a.err = err;
   return cuda_status(launch_swa_append(a, s.batch, stream));
 }
 
@@ -623,6 +659,26 @@ int csa2_read_device_error(void* ws, csa2_stream_t stream, int32_t* detail) {
 }
 
 unsigned long long csa2_launch_count(void) { return g_launches.load(std::memory_order_relaxed); }
+
+int csa2_debug_wait_timeout(const csa2_shape* shape, const void* q_idx, const float* w, const void* k_idx,
+                            const int32_t* n_valid, int32_t k, int32_t* idx_out, uint32_t wait_limit_ns, void* ws,
+                            size_t ws_bytes, csa2_stream_t stream) {
+  CSA2_TRY(check_shape(shape));
+  const csa2_shape& s = *shape;
+  CSA2_TRY(check_ws(s, ws, ws_bytes));
+  if (q_idx == nullptr || w == nullptr || k_idx == nullptr || n_valid == nullptr || idx_out == nullptr || k < 1 ||
+      k > s.topk)
+    return CSA2_ERR_INVALID_ARG;
+  if (wait_limit_ns < 1000u || wait_limit_ns > 100000000u) return CSA2_ERR_INVALID_ARG;
+  if (!indexer_fast(s) || !index_select_supported(false, s.n_entries) || !aligned16(k_idx))
+    return CSA2_ERR_UNSUPPORTED;
+  const WsLayout L = layout(s);
+  SelectArgs a = select_args(s, k_idx, s.n_entries, seqdiv(s), q_idx, w, n_valid, 1, k, idx_out, k, nullptr,
+                             at<int>(ws, L.hdr));
+  a.wait_ns = wait_limit_ns;
+  a.skip_first_copy = 1;
+  return cuda_status(launch_index_select(a, false, s.batch, s.n_entries, stream));
+}
 
 int csa2_fast_path(const csa2_shape* shape, int32_t* indexer_fast_out, int32_t* attention_fast_out) {
   if (check_shape(shape) != CSA2_OK) return 0;

@@ -456,12 +456,10 @@ cudaError_t launch_attn(const AttnArgs& a, bool fast, int batch, cudaStream_t st
     note_launch();
     return launch_pdl(attn_generic_kernel, grid, dim3(128), smem, st, 1, a);
   }
-  static bool attr_set = false;
-  if (!attr_set) {
-    cudaError_t e = cudaFuncSetAttribute(attn_mma_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
-    if (e != cudaSuccess) return e;
-    attr_set = true;
-  }
+  const cudaError_t e = once_per_device(kSetupAttn, [] {
+    return cudaFuncSetAttribute(attn_mma_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+  });
+  if (e != cudaSuccess) return e;
   const int ncta = attn_cluster(a.topk, a.swa);
   if (ncta == 0) return cudaErrorInvalidValue;
   note_launch();

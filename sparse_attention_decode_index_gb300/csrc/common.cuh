@@ -79,13 +79,18 @@ CSA2_DEV bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
   return done != 0;
 }
 
-// Wait for the given phase parity; gives up after ~2 s and returns false.
-CSA2_DEV bool mbar_wait(uint64_t* bar, uint32_t parity) {
+// Default limit of a bounded wait: 2 s.
+constexpr uint64_t kWaitLimitNs = 2000000000ull;
+
+// Wait for the given phase parity; gives up after `limit_ns` (0: the default
+// 2 s) and returns false.
+CSA2_DEV bool mbar_wait(uint64_t* bar, uint32_t parity, uint64_t limit_ns = 0) {
   if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t limit = limit_ns != 0 ? limit_ns : kWaitLimitNs;
   const uint64_t t0 = global_ns();
   for (uint32_t i = 1;; ++i) {
     if (mbar_try_wait(bar, parity)) return true;
-    if ((i & 255u) == 0u && global_ns() - t0 > 2000000000ull) return false;
+    if ((i & 31u) == 0u && global_ns() - t0 > limit) return false;
   }
 }
 

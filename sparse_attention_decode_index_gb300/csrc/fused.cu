@@ -39,6 +39,8 @@
 //
 // (DeepSeek V4.1 Flash architecture page: bullet "Hierarchical indexer" -- block
 // pool, at most 16,384 candidates; bullet "Sparse attention" -- Top-512.)
+#include <mutex>
+
 #include "common.cuh"
 #include "internal.h"
 
@@ -97,6 +99,7 @@ struct SelSmall {
   uint32_t gt_g[kMaxCluster];      // rank finish: per CTA, gathered keys above / at the threshold
   uint32_t eq_g[kMaxCluster];
   uint32_t sel_bin, sel_above, gcount;
+  uint32_t failed;                 // a bounded wait of this CTA gave up
   uint64_t full[kStages];
   uint64_t empty[kStages];
 };
@@ -187,6 +190,7 @@ __global__ void __launch_bounds__(kThreads, 4) index_select_kernel(const SelectA
       mbar_init(&sm.empty[s], kConsumers);
     }
     mbar_fence_init();
+    sm.failed = 0u;
   }
   pdl_wait();   // the pool / n_pool come from the preceding launch
   const int nv = clamp_count(a.n_valid[b], a.valid_cap, a.err);
@@ -223,15 +227,16 @@ __global__ void __launch_bounds__(kThreads, 4) index_select_kernel(const SelectA
     for (; i < ntiles; ++i) {
       const int s = i % kStages;
       bool ok = true;
-      if (lane == 0 && i >= kStages) ok = mbar_wait(&sm.empty[s], ((i / kStages) - 1) & 1);
+      if (lane == 0 && i >= kStages) ok = mbar_wait(&sm.empty[s], ((i / kStages) - 1) & 1, a.wait_ns);
       if (!__shfl_sync(0xffffffffu, ok, 0)) break;
       uint8_t* dst = tiles + s * kTileBytes;
+      const bool copy = !(a.skip_first_copy && i == 0);   // test hook: tile 0's barrier never completes
       if (!POOLED) {
         if (lane == 0) {
           const int r0 = begin + i * kTileRows;
           const uint32_t bytes = uint32_t(min(kTileRows, end - r0)) * kRowBytes;
           mbar_arrive_expect_tx(&sm.full[s], bytes);
-          bulk_g2s(dst, keys + (long long)r0 * kRowBytes, bytes, &sm.full[s]);
+          if (copy) bulk_g2s(dst, keys + (long long)r0 * kRowBytes, bytes, &sm.full[s]);
         }
       } else {
         const int p0 = i * kBlocksPerTile;
@@ -240,13 +245,18 @@ __global__ void __launch_bounds__(kThreads, 4) index_select_kernel(const SelectA
         const unsigned have = __ballot_sync(0xffffffffu, blk >= 0);
         if (lane == 0) mbar_arrive_expect_tx(&sm.full[s], uint32_t(__popc(have)) * kBlockBytes);
         __syncwarp();
-        if (blk >= 0)
+        if (blk >= 0 && copy)
           bulk_g2s(dst + lane * kBlockBytes, keys + (long long)blk * kBlockBytes, kBlockBytes, &sm.full[s]);
       }
     }
     if (lane == 0) {
-      if (i < ntiles) report(a.err, kErrTimeout, i);
-      for (int j = max(0, i - kStages); j < i; ++j) mbar_wait(&sm.full[j % kStages], (j / kStages) & 1);
+      if (i < ntiles) {
+        report(a.err, kErrTimeout, i);
+        sm.failed = 1u;
+      }
+      // every copy issued has landed (or its wait gave up) before the ring is reused
+      for (int j = max(0, i - kStages); j < i; ++j)
+        if (!mbar_wait(&sm.full[j % kStages], (j / kStages) & 1, a.wait_ns)) sm.failed = 1u;
     }
   } else {
     const int g = lane >> 2, t = lane & 3;
@@ -259,8 +269,9 @@ __global__ void __launch_bounds__(kThreads, 4) index_select_kernel(const SelectA
     const bool relu = a.relu != 0;
     for (int i = 0; i < ntiles; ++i) {
       const int s = i % kStages;
-      if (!mbar_wait(&sm.full[s], (i / kStages) & 1)) {
+      if (!mbar_wait(&sm.full[s], (i / kStages) & 1, a.wait_ns)) {
         report(a.err, kErrTimeout, i);
+        sm.failed = 1u;
         break;
       }
       const uint8_t* tile = tiles + s * kTileBytes;
@@ -319,6 +330,16 @@ __global__ void __launch_bounds__(kThreads, 4) index_select_kernel(const SelectA
   }
   if (tid < 3 && rows_total + tid < key_words(rows_total)) s_key[rows_total + tid] = 0u;   // padding: no candidate
   __syncthreads();   // all keys written; the ring buffer is free for the histogram
+  if (sm.failed) {
+    // A bounded wait gave up (recorded in the error word): some keys were never
+    // written.  This CTA then offers no candidate, so that the cluster's
+    // selection stays consistent and every write stays in bounds.
+    for (int j = tid; j < key_words(rows_total); j += kThreads) s_key[j] = 0u;
+    my_cnt = 0u;
+    my_lo = 0xffffffffu;
+    my_hi = 0u;
+    __syncthreads();
+  }
 
   // ---------------- phase 2: cluster-wide exact Top-k over the keys
   uint32_t* ring = reinterpret_cast<uint32_t*>(smem);
@@ -849,8 +870,6 @@ static cudaError_t choose(bool pooled, int max_units, int batch, ClusterChoice& 
     const int per = (max_units + c - 1) / c;
     if (per * unit_rows > kMaxRowsPerCta) break;
     const size_t smem = select_smem_bytes(per, pooled);
-    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
-    if (e != cudaSuccess) return e;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(unsigned(c), unsigned(batch), 1);
     cfg.blockDim = dim3(kThreads);
@@ -882,36 +901,49 @@ bool index_select_supported(bool pooled, int max_units) {
 
 cudaError_t launch_index_select(const SelectArgs& in, bool pooled, int batch, int max_units, cudaStream_t st) {
   if (batch == 0) return cudaSuccess;
-  // the occupancy query is made once per (device, mode, size, batch)
+  // Every launch may use up to the largest shared-memory size of its mode
+  // (opted in once per device); the cluster choice (an occupancy query) is
+  // made once per (device, mode, size, batch) and kept in a small table
+  // shared by all host threads.
+  cudaError_t e = pooled ? once_per_device(kSetupSelectPooled, [] {
+    return cudaFuncSetAttribute(index_select_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                int(select_smem_bytes(kMaxRowsPerCta / kBlock, true)));
+  }) : once_per_device(kSetupSelectFlat, [] {
+    return cudaFuncSetAttribute(index_select_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                int(select_smem_bytes(kMaxRowsPerCta, false)));
+  });
+  if (e != cudaSuccess) return e;
   struct Entry {
     int dev, pooled, units, batch;
     ClusterChoice ch;
   };
   static Entry cache[16];
   static int n_cache = 0;
+  static std::mutex mu;
   int dev = 0;
-  cudaGetDevice(&dev);
+  e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
   ClusterChoice ch;
-  bool hit = false;
-  for (int i = 0; i < n_cache; ++i)
-    if (cache[i].dev == dev && cache[i].pooled == int(pooled) && cache[i].units == max_units &&
-        cache[i].batch == batch) {
-      ch = cache[i].ch;
-      hit = true;
+  {
+    std::lock_guard<std::mutex> lock(mu);
+    bool hit = false;
+    for (int i = 0; i < n_cache && i < 16; ++i)
+      if (cache[i].dev == dev && cache[i].pooled == int(pooled) && cache[i].units == max_units &&
+          cache[i].batch == batch) {
+        ch = cache[i].ch;
+        hit = true;
+      }
+    if (!hit) {
+      e = choose(pooled, max_units, batch, ch);
+      if (e != cudaSuccess) return e;
+      cache[n_cache % 16] = Entry{dev, int(pooled), max_units, batch, ch};
+      ++n_cache;
     }
-  cudaError_t e = cudaSuccess;
-  if (!hit) {
-    e = choose(pooled, max_units, batch, ch);
-    if (e != cudaSuccess) return e;
-    cache[n_cache % 16] = Entry{dev, int(pooled), max_units, batch, ch};
-    ++n_cache;
   }
   if (ch.c == 0) return cudaErrorInvalidValue;
   SelectArgs a = in;
   a.rows_per_cta = ch.units_per_cta;
   auto kern = pooled ? index_select_kernel<true> : index_select_kernel<false>;
-  e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, int(ch.smem));
-  if (e != cudaSuccess) return e;
   note_launch();
   return launch_pdl(kern, dim3(unsigned(ch.c), unsigned(batch), 1), dim3(kThreads), ch.smem, st, unsigned(ch.c), a);
 }

@@ -18,6 +18,8 @@
 // contiguous bytes of a row that its fragment needs: the dim order inside a
 // k-step is permuted identically for the A (keys) and B (q_idx) fragments,
 // which leaves the dot products unchanged, so no ldmatrix or swizzle is needed.
+#include <atomic>
+
 #include "common.cuh"
 #include "internal.h"
 
@@ -279,19 +281,20 @@ __global__ void __launch_bounds__(256) block_keys_kernel(const BlockKeyArgs a) {
   store_elem(a.kb, ((long long)b * a.nb_cap + j) * a.dim + d, a.dtype, v);
 }
 
-int g_sm_count[64];
+std::atomic<int> g_sm_count[64];
 
 }  // namespace
 
 int device_sm_count() {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 148;
-  if (g_sm_count[dev] == 0) {
-    int n = 0;
+  int n = g_sm_count[dev].load(std::memory_order_relaxed);
+  if (n == 0) {
     cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
-    g_sm_count[dev] = n > 0 ? n : 148;
+    if (n <= 0) n = 148;
+    g_sm_count[dev].store(n, std::memory_order_relaxed);
   }
-  return g_sm_count[dev];
+  return n;
 }
 
 cudaError_t launch_block_keys(const BlockKeyArgs& a, int batch, cudaStream_t st) {
@@ -315,13 +318,15 @@ cudaError_t launch_indexer(const IndexerArgs& in, bool pooled, bool fast, int ba
     return launch_pdl(indexer_generic_kernel, grid, dim3(256), smem, st, 1, a, pooled ? 1 : 0);
   }
   const size_t smem = fast_smem_bytes(pooled);
-  static bool attr_set[2] = {false, false};
   auto kern = pooled ? indexer_mma_kernel<true> : indexer_mma_kernel<false>;
-  if (!attr_set[pooled]) {
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
-    if (e != cudaSuccess) return e;
-    attr_set[pooled] = true;
-  }
+  const cudaError_t e = pooled ? once_per_device(kSetupIndexerPooled, [] {
+    return cudaFuncSetAttribute(indexer_mma_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                int(fast_smem_bytes(true)));
+  }) : once_per_device(kSetupIndexerFlat, [] {
+    return cudaFuncSetAttribute(indexer_mma_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                int(fast_smem_bytes(false)));
+  });
+  if (e != cudaSuccess) return e;
   int per_sm = 1;
   cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, kThreads, smem);
   if (per_sm < 1) per_sm = 1;

@@ -92,6 +92,13 @@ struct SelectArgs {
   long long ld_out;
   int* n_out;                // [B] number selected (nullable)
   int* err;
+  // Test hooks of the bounded waits (0 in every production launch): a limit
+  // for every mbarrier wait instead of the default 2 s, and a flag that
+  // leaves out the copy of each CTA's first tile, so that the tile's stage
+  // barrier cannot complete and the waits run out (no copy is in flight
+  // when they give up).
+  unsigned long long wait_ns;
+  int skip_first_copy;
 };
 
 bool index_select_supported(bool pooled, int max_units);
@@ -143,6 +150,10 @@ cudaError_t launch_swa_append(const SwaAppendArgs& a, int batch, cudaStream_t st
 
 int device_sm_count();
 
+// Device address of the library's static scratch array (static_ws.cu) on the
+// current device, looked up once per device; CSA2_OK or CSA2_ERR_CUDA.
+int static_scratch(void** out);
+
 // Launch `kernel` with programmatic stream serialization (PDL) and an optional
 // cluster shape; every kernel of the library calls pdl_wait() before touching
 // data of earlier launches.
@@ -172,6 +183,13 @@ cudaError_t launch_pdl(void (*kernel)(Params...), dim3 grid, dim3 block, size_t 
 }
 // Counts kernel launches enqueued by the library (diagnostics: csa2_launch_count).
 void note_launch();
+
+// Per-device one-time set-up (a kernel's shared-memory opt-in is a per-device
+// attribute): runs `set` with the current device current the first time `key`
+// (0..63) is seen on that device, and again until it succeeds.  Thread-safe.
+enum SetupKey { kSetupAttn = 0, kSetupIndexerFlat = 1, kSetupIndexerPooled = 2, kSetupSelectFlat = 3,
+                kSetupSelectPooled = 4 };
+cudaError_t once_per_device(int key, cudaError_t (*set)());
 
 cudaError_t launch_block_keys(const BlockKeyArgs& a, int batch, cudaStream_t st);
 // fast: bf16, 8 heads x 64 dims, block 8 (pooled)

@@ -31,6 +31,10 @@ plus a 128-token SWA window, blocks of 8, a pool of at most 2,048 blocks):
 * ``enc_stack_b32_32k`` -- the whole 20-layer encoder stack SWA, SWA,
   [Full + 5 Reuse] x 3 at the shapes of ``enc_b32_32k`` (pure SWA layers attend
   their window only).
+* ``dec_b64_128k`` -- the decoder group of ``dec_b16_1m`` at the context and
+  batch of ``reindex_b64_128k`` (batch 64, 32,768 entries, pool of 2,048).
+* ``replay_t128_128k`` -- one sequence's last 128 prompt tokens through the
+  decoder group at 128K context, caches shared by the tokens.
 
 Value recipe: main and SWA keys N(0,1)/sqrt(k_dim), values
 N(0,1)/sqrt(v_dim), queries N(0,1), all rounded to bf16; indexer queries
@@ -300,6 +304,9 @@ WORKLOADS = {
                               context=32768),
     "dec_b16_1m": dict(cfg_id=4, batch=16, n_entries=262144, modes=decoder_group_modes(),
                        pool=2048, context=1048576),
+    # the 20-layer decoder group at the 128K Reindex workload's context and batch
+    "dec_b64_128k": dict(cfg_id=7, batch=64, n_entries=32768, modes=decoder_group_modes(), pool=2048,
+                         context=131072),
     # one sequence's 128-token decoder replay through the 20-layer decoder group at 128K context
     "replay_t128_128k": dict(cfg_id=6, sequences=1, tokens=128, n_entries=32768, modes=decoder_group_modes(),
                              pool=2048, context=131072),

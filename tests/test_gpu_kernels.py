@@ -379,3 +379,27 @@ def test_index_topk_pooled_wide_or_negative_scores(csa2, case):
                                  block=8, pool=P, hier=True, relu=case != "relu_off")
         assert got[b].tolist() == r["idx"].tolist(), f"{case} query {b}"
     assert_no_device_error(csa2, ws)
+
+
+# ------------------------------------------------------------------ bounded device waits
+
+def test_bounded_wait_gives_up_and_reports_timeout(csa2):
+    """A stage barrier that nothing completes (csa2_debug_wait_timeout leaves out the copy
+    of every CTA's first tile): the waits give up after 20 us, the kernel returns, the
+    error word says CSA2_ERR_TIMEOUT (bit 2), every write stayed inside the output, and
+    the same workspace and stream then serve a normal call that matches the oracle."""
+    sh = _shape(batch=4, n_entries=4096, pool_blocks=0)
+    wl = W.make_workload(sh, [W.FULL], seed=3, cfg_id=61, n_valid=[4096, 4000, 700, 64])
+    d = csa2.upload(wl)
+    L = d["layers"][0]
+    assert_no_device_error(csa2, d["ws"])
+    idx = torch.full((sh.batch, sh.topk), -7, dtype=torch.int32, device="cuda")
+    csa2.debug_wait_timeout(sh, L["q_idx"], L["w_idx"], d["k_idx"], d["n_valid"], sh.topk, idx, 20000, d["ws"])
+    st, bits = csa2.read_device_error(d["ws"])
+    assert st == -6 and bits & 4, (st, bits)          # CSA2_ERR_TIMEOUT
+    # every CTA gave up on its first tile and offered no candidate
+    assert np.all(idx.cpu().numpy() == -1)
+    csa2.index_topk(sh, L["q_idx"], L["w_idx"], d["k_idx"], d["n_valid"], sh.topk, idx, d["ws"])
+    ref = oracle.run_group(wl, want_attention=False)[0]["idx"]
+    assert np.array_equal(idx.cpu().numpy(), ref)
+    assert_no_device_error(csa2, d["ws"])

@@ -19,7 +19,9 @@ PINS = [P.test_golden_toy16_hand, P.test_indexer_scores_match_integer_loops,
         lambda: P.test_sparse_equals_dense_causal_attention_naive(24, 8, 16),
         P.test_kv_append_in_steps_equals_the_cache_written_at_once,
         P.test_kv_append_touches_only_the_blocks_of_the_new_positions,
-        P.test_swa_ring_holds_the_last_w_tokens]
+        P.test_swa_ring_holds_the_last_w_tokens,
+        P.test_block_keys_stored_as_bf16_round_the_mean_to_nearest_even,
+        P.test_tokens_of_one_sequence_see_their_own_partial_last_block]
 
 
 def _topk_highest_id_wins(scores, ids, k):
@@ -70,6 +72,31 @@ def _pool_unsorted(q_idx, w, kb, n_blocks, pool, relu=True):
     return order[:min(pool, n_blocks)]
 
 
+def _block_keys_bf16_truncated(keys, n_valid, block, round_to_int, store_bf16=False):
+    nb = -(-n_valid // block)
+    out = np.zeros((nb, keys.shape[1]))
+    for j in range(nb):
+        rows = keys[j * block: min((j + 1) * block, n_valid)]
+        m = rows.sum(axis=0) / rows.shape[0]
+        if round_to_int:
+            m = np.rint(m)
+        elif store_bf16:
+            mm, e = np.frexp(m)
+            m = np.ldexp(np.trunc(mm * 256.0), e - 8)
+        out[j] = m
+    return out
+
+
+def _block_keys_bf16_not_rounded(keys, n_valid, block, round_to_int, store_bf16=False):
+    return _orig_block_keys(keys, n_valid, block, round_to_int, store_bf16=False)
+
+
+def _block_keys_whole_cache(keys, n_valid, block, round_to_int, store_bf16=False):
+    # a token's summary keys taken over its sequence's whole cache, not its own valid prefix
+    return _orig_block_keys(keys, keys.shape[0], block, round_to_int, store_bf16=store_bf16)
+
+
+_orig_block_keys = C.block_keys
 _orig_attend = C.attend
 _orig_kv_append = C.kv_append
 _orig_swa_append = C.swa_append
@@ -111,6 +138,9 @@ MUTATIONS = {
     "appended entries land one slot late": ("kv_append", _kv_append_one_slot_late),
     "summary key of a newly opened block not computed": ("kv_append", _kv_append_stale_last_block),
     "SWA ring head never advances": ("swa_append", _swa_append_head_stuck),
+    "bf16 block means truncated instead of rounded": ("block_keys", _block_keys_bf16_truncated),
+    "bf16 block means stored unrounded": ("block_keys", _block_keys_bf16_not_rounded),
+    "a token's block keys taken over the whole cache": ("block_keys", _block_keys_whole_cache),
 }
 
 

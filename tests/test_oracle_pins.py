@@ -108,6 +108,25 @@ def test_block_keys_rounding_half_even_and_partial_block():
     assert kb[:, 0].tolist() == [0.5, 1.5, -0.5, -1.5, 2.0]      # n_valid = 9: last block = entry 8
 
 
+def test_block_keys_stored_as_bf16_round_the_mean_to_nearest_even():
+    """Unrounded block means stored as bf16 (the fp32-free path of the summary keys): the mean
+    of the block's valid keys, computed exactly, then rounded once to bf16, ties to even.
+    Hand values (bf16 keeps 8 significant bits; the step above 1 is 2^-7):
+      [1, 1 + 2^-7]        -> 1 + 2^-8, halfway between 1 and 1 + 2^-7      -> 1 (even)
+      [1, 1 + 3 * 2^-7]    -> 1 + 1.5 * 2^-7, halfway                        -> 1 + 2^-6 (even)
+      [2, 3]               -> 2.5, a bf16 value                              -> 2.5
+      [1, 1, 2] (partial)  -> 4/3 = 1.0101...b; 8 bits keep 1 + 43 * 2^-7    -> 1.3359375"""
+    keys = np.array([1.0, 1 + 2 ** -7, 1.0, 1 + 3 * 2 ** -7, 2.0, 3.0, 1.0, 1.0, 2.0], dtype=np.float64)
+    # blocks of 2 over the first 6 keys, then a block of 4 holding 3 valid keys
+    kb2 = oracle.block_keys(keys[:6, None], 6, 2, round_to_int=False, store_bf16=True)
+    assert kb2[:, 0].tolist() == [1.0, 1 + 2 ** -6, 2.5]
+    kb4 = oracle.block_keys(keys[6:, None], 3, 4, round_to_int=False, store_bf16=True)
+    assert kb4[:, 0].tolist() == [1 + 43 * 2 ** -7]
+    # without bf16 storage the plain means come back
+    kb2f = oracle.block_keys(keys[:6, None], 6, 2, round_to_int=False, store_bf16=False)
+    assert kb2f[:, 0].tolist() == [1 + 2 ** -8, 1 + 1.5 * 2 ** -7, 2.5]
+
+
 def test_bf16_decode_and_rounding():
     bits = np.array([0x3F80, 0xC000, 0x3FC0, 0x0000, 0x4080, 0xBE00], dtype=np.uint16)
     assert oracle.to_f64(bits).tolist() == [1.0, -2.0, 1.5, 0.0, 4.0, -0.125]
@@ -429,3 +448,31 @@ def test_decoder_replay_shares_caches_and_slides_the_windows():
     a, b = oracle.run_group(wl, queries=qs), oracle.run_group(flat, queries=qs)
     for x, y in zip(a, b):
         assert np.array_equal(x["idx"], y["idx"]) and np.array_equal(x["out"], y["out"])
+
+
+def test_tokens_of_one_sequence_see_their_own_partial_last_block():
+    """Two query tokens of one sequence (shape.tokens = 2) share its indexer keys but have
+    different causal counts, so their partial last blocks differ.  Hand case, blocks of 2,
+    a pool of one block, Top-1, one indexer head with q = w = 1 (score = the key):
+      keys 1, 1, 0, 9, 5, 5
+      token 0, n_valid 3: block keys 1, 0 (its last block holds entry 2 only) -> pool [0]
+                          -> candidates 0, 1 (scores 1, 1) -> Top-1 [0] (tie: lowest id)
+      token 1, n_valid 4: block keys 1, rint(4.5) = 4 -> pool [1] -> candidates 2, 3
+                          (scores 0, 9) -> Top-1 [3]
+    Block keys taken over the sequence's whole cache would give token 0 the pool [1]
+    and the index [2] (entry 3 lies past its n_valid)."""
+    sh = W.Shape(batch=2, n_entries=6, idx_heads=1, idx_dim=1, block=2, pool_blocks=1, topk=1, q_heads=1,
+                 k_dim=1, v_dim=1, swa=1, dtype="f32", tokens=2)
+    one = np.ones((2, 1, 1), dtype=np.float32)
+    layer = W.Layer(mode=REINDEX, hier=1, q=one, k_swa=one.copy(), v_swa=one.copy(), q_idx=one.copy(),
+                    w_idx=np.ones((2, 1), dtype=np.float32))
+    keys = np.array([1, 1, 0, 9, 5, 5], dtype=np.float32)[None, :, None]
+    wl = W.Workload(name="tokens_hand", shape=sh, k_main=keys.copy(), v_main=keys.copy(), k_idx=keys,
+                    n_valid=np.array([3, 4], dtype=np.int32), n_swa=np.array([0, 0], dtype=np.int32),
+                    layers=[layer], round_block_keys=1)
+    r = oracle.run_group(wl)[0]
+    assert [p.tolist() for p in r["pool"]] == [[0], [1]]
+    assert [c.tolist() for c in r["cand"]] == [[0, 1], [2, 3]]
+    assert r["idx"].tolist() == [[0], [3]]
+    # attention reads the selected entry's K/V (no window): out = its value row
+    assert r["out"][:, 0, 0].tolist() == [1.0, 9.0]
