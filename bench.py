@@ -382,7 +382,6 @@ def run_ours(args):
                     graph.replay()
                 torch.cuda.synchronize()
 
-        csa2.debug_select_counters(d["ws"], stream)          # clear the fused selection counters
         with ClockSampler(dev.index) as clk:
             soak(args.clock_soak)
             barrier()
@@ -396,7 +395,6 @@ def run_ours(args):
             barrier()
             soak(args.clock_soak / 2)
         step_ms = [e0.elapsed_time(e1) for e0, e1 in evs]
-        sel, fb = csa2.debug_select_counters(d["ws"], stream)
     total_s = max_over_ranks(sum(step_ms) / 1e3, dev)
     value = sh.batch * world * args.steps / total_s
     ms_per_step = 1e3 * total_s / args.steps
@@ -423,9 +421,6 @@ def run_ours(args):
                 "cpu_baseline": cpu, "e2e": e2e, "append": append,
                 "gpu_launches": per_step_launches * args.steps,
                 "launches_per_step": per_step_launches, "clocks": clocks,
-                "selection": {"fused_selections": sel, "radix_fallbacks": fb,
-                              "note": "per-query fused selections over the soak and timed steps; fallbacks: "
-                                      "the sampled key bracket missed and the exact radix passes ran"},
                 "step_ms": {"median": statistics.median(step_ms), "min": min(step_ms), "max": max(step_ms)}}
         print(json.dumps(line))
     if world > 1:

@@ -322,14 +322,6 @@ int csa2_fast_path(const csa2_shape* shape, int32_t* indexer_fast, int32_t* atte
  * at capture).  For diagnostics and launch accounting. */
 unsigned long long csa2_launch_count(void);
 
-/* Selection diagnostics (the paper has no counterpart).  Synchronises
- * `stream`, then reads and clears two counters in the workspace header that
- * the fused scoring + Top-k kernel keeps: *selections, the per-query
- * selections it ran with more candidates than k, and *fallbacks, those of
- * them that its sampled key bracket did not settle, so that its exact radix
- * passes ran instead.  Either output pointer may be NULL. */
-int csa2_debug_select_counters(void* ws, csa2_stream_t stream, uint32_t* selections, uint32_t* fallbacks);
-
 /* Test hook of the device-side failure detection (diagnostics; the paper has
  * no counterpart).  Runs the fused flat scoring + Top-k of csa2_index_topk
  * (pool == NULL; fast path only, else CSA2_ERR_UNSUPPORTED) with the copy of

@@ -72,8 +72,6 @@ _SIGS = {
     "csa2_layer_group_static": (ctypes.c_int, [ctypes.POINTER(CShape), ctypes.POINTER(CLayer), _I32, _VP, _VP,
                                                _VP, _VP, _VP, _VP, _VP]),
     "csa2_read_static_device_error": (ctypes.c_int, [_VP, ctypes.POINTER(_I32)]),
-    "csa2_debug_select_counters": (ctypes.c_int, [_VP, _VP, ctypes.POINTER(ctypes.c_uint32),
-                                                  ctypes.POINTER(ctypes.c_uint32)]),
     "csa2_debug_wait_timeout": (ctypes.c_int, [ctypes.POINTER(CShape), _VP, _VP, _VP, _VP, _I32, _VP, ctypes.c_uint32,
                                                _VP, _SZ, _VP]),
 }
@@ -335,15 +333,6 @@ def read_static_device_error(stream=None):
     d = _I32(0)
     st = lib().csa2_read_static_device_error(_stream(stream), ctypes.byref(d))
     return int(st), int(d.value)
-
-
-def debug_select_counters(ws, stream=None):
-    """Synchronise, read and clear the fused selection counters of a workspace:
-    (selections run, selections the sampled bracket did not settle)."""
-    a, b = ctypes.c_uint32(0), ctypes.c_uint32(0)
-    _check(lib().csa2_debug_select_counters(_ptr(ws, torch.uint8, "ws"), _stream(stream), ctypes.byref(a),
-                                            ctypes.byref(b)), "csa2_debug_select_counters")
-    return int(a.value), int(b.value)
 
 
 def debug_wait_timeout(shape, q_idx, w, k_idx, n_valid, k: int, idx_out, wait_limit_ns: int, ws, stream=None):

@@ -660,20 +660,6 @@ int csa2_read_device_error(void* ws, csa2_stream_t stream, int32_t* detail) {
 
 unsigned long long csa2_launch_count(void) { return g_launches.load(std::memory_order_relaxed); }
 
-int csa2_debug_select_counters(void* ws, csa2_stream_t stream, uint32_t* selections, uint32_t* fallbacks) {
-  if (ws == nullptr) return CSA2_ERR_WORKSPACE;
-  uint32_t host[2] = {0u, 0u};
-  uint32_t* words = static_cast<uint32_t*>(ws) + kCounterSelections;
-  static_assert(kCounterFallbacks == kCounterSelections + 1, "adjacent counters");
-  if (cudaMemcpyAsync(host, words, sizeof(host), cudaMemcpyDeviceToHost, stream) != cudaSuccess) return CSA2_ERR_CUDA;
-  if (cudaStreamSynchronize(stream) != cudaSuccess) return CSA2_ERR_CUDA;
-  if (cudaMemsetAsync(words, 0, sizeof(host), stream) != cudaSuccess) return CSA2_ERR_CUDA;
-  if (cudaStreamSynchronize(stream) != cudaSuccess) return CSA2_ERR_CUDA;
-  if (selections != nullptr) *selections = host[0];
-  if (fallbacks != nullptr) *fallbacks = host[1];
-  return CSA2_OK;
-}
-
 int csa2_debug_wait_timeout(const csa2_shape* shape, const void* q_idx, const float* w, const void* k_idx,
                             const int32_t* n_valid, int32_t k, int32_t* idx_out, uint32_t wait_limit_ns, void* ws,
                             size_t ws_bytes, csa2_stream_t stream) {

@@ -83,16 +83,6 @@ constexpr int kCopiesL = 8;
 constexpr int kLocalWords = kBins * kCopiesL + kBins;               // local histogram + totals
 constexpr int kBinWords = kMaxRowsPerCta / 4;
 constexpr int kGatherWords = kRegionA - kLocalWords;                // gather buffer capacity
-// The sampled bracket: the first kSampleTiles tiles of every CTA's rows are a
-// sample of the query's candidates.  Every CTA pushes its sample into every
-// CTA; kBracketLag tiles later all CTAs turn the (identical) sample into the
-// same key bracket around the expected k-th largest key.
-constexpr int kSampleTiles = 2;
-constexpr int kSampleRows = kSampleTiles * kTileRows;                // 128 rows per CTA
-constexpr int kSampleWords = kMaxCluster * kSampleRows;              // 1,024 keys at most
-constexpr int kBracketLag = 2;
-static_assert(kMTiles == 1, "a consumer warp owns one 16-row group of every tile");
-static_assert(kBins / 2 == kConsumers * 32, "one bracket histogram word per consumer thread");
 
 static_assert(kHistDWords <= kGatherWords, "histogram fits region A below its tail");
 static_assert(kBinWords <= kLocalWords, "key bins fit the tail of region A");
@@ -101,10 +91,7 @@ static_assert(kMaxRowsPerCta < 65536, "16-bit histogram counters");
 
 struct SelSmall {
   uint4 stats[kMaxCluster];        // pushed by every CTA: (keys, min key, max key, 0)
-  uint4 bstats[kMaxCluster];       // pushed by every CTA: (keys above the bracket, keys in it, bracket usable, 0)
-  uint32_t red[5][kWarpsAll];
-  uint32_t bred[3][kConsumers];    // bracket: per consumer warp (sample count, min, max)
-  uint32_t br_ok;                  // this CTA's bracket is usable
+  uint32_t red[3][kWarpsAll];
   uint32_t above_r[kMaxCluster];   // per CTA: keys above the current range
   uint32_t cnt_r[kMaxCluster];     // per CTA: keys inside the current range
   uint32_t gt_r[kMaxCluster];      // per CTA: keys above the threshold
@@ -178,147 +165,10 @@ constexpr size_t kOffKeys = kOffSmall + ((sizeof(SelSmall) + 127) / 128) * 128;
 
 // Keys are stored in a multiple of 4 words so that 16-byte reads stay inside them.
 __host__ __device__ constexpr int key_words(int rows) { return (rows + 3) & ~3; }
-// Words of a one-bit-per-row map, a multiple of 4.
-__host__ __device__ constexpr int map_words(int rows) { return ((rows + 31) / 32 + 3) & ~3; }
 
-// Shared memory after the ring and the small state: the order keys, the pool
-// slice (pooled), the bracket sample, its histogram (16-bit counters, two per
-// word) and the row maps of the keys above the bracket and inside it.
-struct SelLayout {
-  size_t keys, pool, samp, hist, above, inside, total;
-};
-
-__host__ __device__ constexpr size_t align16(size_t x) { return (x + 15) & ~size_t(15); }
-
-__host__ __device__ SelLayout sel_layout(int units, bool pooled) {
-  const int rows = pooled ? units * kBlock : units;
-  SelLayout L{};
-  L.keys = kOffKeys;
-  L.pool = L.keys + size_t(key_words(rows)) * 4;
-  L.samp = align16(L.pool + (pooled ? size_t(units) * 4 : 0));
-  L.hist = L.samp + size_t(kSampleWords) * 4;
-  L.above = L.hist + size_t(kBins / 2) * 4;
-  L.inside = L.above + size_t(map_words(rows)) * 4;
-  L.total = L.inside + size_t(map_words(rows)) * 4;
-  return L;
-}
-
-size_t select_smem_bytes(int rows_per_cta, bool pooled) { return sel_layout(rows_per_cta, pooled).total; }
-
-// ---------------------------------------------------------------- the sampled bracket
-
-// Key classes of the bracket: keys above it (all selected when the bracket
-// holds), keys inside it (gathered for the exact finish), keys below it.
-constexpr uint32_t kBelow = 0u, kInside = 1u, kAbove = 2u;
-
-struct Bracket {
-  uint32_t smin, smax;   // sample key range; bins are taken over it
-  Binning bn;
-  int b_lo, b_hi;        // inside: bins b_lo .. b_hi (keys below smin: bin -1, above smax: bin 256)
-};
-
-__device__ __forceinline__ void consumer_sync() {
-  asm volatile("bar.sync 1, %0;" ::"n"(kConsumers * 32) : "memory");
-}
-
-// Class of an order key (0 = not a candidate is below everything).  The
-// extended bin is non-decreasing in the key, so the classes are contiguous
-// key ranges: every key above the bracket exceeds every key inside it.
-__device__ __forceinline__ uint32_t classify(uint32_t kk, const Bracket& br) {
-  if (kk == 0u) return kBelow;
-  const int e = kk < br.smin ? -1 : (kk > br.smax ? kBins : int(bin_of(kk, br.bn)));
-  return e > br.b_hi ? kAbove : (e >= br.b_lo ? kInside : kBelow);
-}
-
-// The bracket from the cluster's sample, nsamp = C * kSampleRows keys (consumer
-// warps only; every CTA gets the same sample and computes the same bracket).  With ns valid sample keys
-// out of about n_est candidates, the k-th largest key is expected near sample
-// rank r = k * ns / n_est (counted from the top); the bracket spans sample
-// ranks r -/+ (4 sqrt(r) + 4), widened to whole histogram bins.  An unusable
-// sample yields an empty bracket (b_lo > b_hi) and *ok = false.
-__device__ Bracket make_bracket(const uint32_t* samp, int nsamp, uint32_t* hist, SelSmall& sm, float kf, float nf,
-                                int ctid, int lane, int warp, bool* ok) {
-  cluster_wait();   // every CTA's sample has landed in samp
-  hist[ctid] = 0u;
-  uint32_t c = 0u, mn = 0xffffffffu, mx = 0u;
-  for (int j = ctid; j < nsamp; j += kConsumers * 32) {
-    const uint32_t v = samp[j];
-    if (v != 0u) {
-      ++c;
-      mn = min(mn, v);
-      mx = max(mx, v);
-    }
-  }
-  c = __reduce_add_sync(0xffffffffu, c);
-  mn = __reduce_min_sync(0xffffffffu, mn);
-  mx = __reduce_max_sync(0xffffffffu, mx);
-  if (lane == 0) {
-    sm.bred[0][warp] = c;
-    sm.bred[1][warp] = mn;
-    sm.bred[2][warp] = mx;
-  }
-  consumer_sync();
-  Bracket br{};
-  uint32_t ns = 0u;
-  br.smin = 0xffffffffu;
-  br.smax = 0u;
-  for (int w = 0; w < kConsumers; ++w) {
-    ns += sm.bred[0][w];
-    br.smin = min(br.smin, sm.bred[1][w]);
-    br.smax = max(br.smax, sm.bred[2][w]);
-  }
-  const float r = (ns > 0u && nf > 0.f) ? kf * float(ns) / nf : 0.f;
-  const float d = 4.f * sqrtf(r) + 4.f;
-  const float r_hi = r - d, r_lo1 = r + d + 1.f;
-  bool use = ns > 0u && r_lo1 <= float(ns) && br.smax > br.smin;
-  br.bn = make_binning(br.smin, br.smax, true);
-  if (use)
-    for (int j = ctid; j < nsamp; j += kConsumers * 32) {
-      const uint32_t v = samp[j];
-      if (v != 0u) {
-        const uint32_t bin = bin_of(v, br.bn);
-        atomicAdd(&hist[bin >> 1], (bin & 1u) ? 0x10000u : 1u);
-      }
-    }
-  consumer_sync();
-  br.b_lo = kBins + 1;   // empty: nothing inside, nothing above
-  br.b_hi = kBins + 1;
-  if (use) {
-    // every warp: lane l holds bins 255 - 8l - j (j = 0..7); bins above it hold `before` samples
-    const int b0 = kBins - 8 - 8 * lane;
-    const uint4 x = *reinterpret_cast<const uint4*>(hist + b0 / 2);   // bins b0 .. b0 + 7
-    const uint32_t g[8] = {x.w >> 16, x.w & 0xffffu, x.z >> 16, x.z & 0xffffu,   // bin b0 + 7 - j
-                           x.y >> 16, x.y & 0xffffu, x.x >> 16, x.x & 0xffffu};
-    uint32_t local = 0u;
-#pragma unroll
-    for (int j = 0; j < 8; ++j) local += g[j];
-    uint32_t incl = local;
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-      const uint32_t y = __shfl_up_sync(0xffffffffu, incl, o);
-      if (lane >= o) incl += y;
-    }
-    uint32_t before = incl - local;
-    int hi_b = kBins, lo_b = -1;
-#pragma unroll
-    for (int j = 0; j < 8; ++j) {
-      const int bin = b0 + 7 - j;
-      const float above = float(before), at = float(before + g[j]);
-      if (above <= r_hi && at > r_hi) hi_b = bin;      // bins above hi_b hold at most r_hi samples
-      if (above < r_lo1 && at >= r_lo1) lo_b = bin;    // bins from lo_b up hold at least r_lo1 samples
-      before += g[j];
-    }
-    hi_b = __reduce_min_sync(0xffffffffu, hi_b);
-    lo_b = __reduce_max_sync(0xffffffffu, lo_b);
-    if (lo_b >= 0) {
-      br.b_lo = lo_b;
-      br.b_hi = hi_b;
-    } else {
-      use = false;
-    }
-  }
-  *ok = use;
-  return br;
+size_t select_smem_bytes(int rows_per_cta, bool pooled) {
+  const int rows = pooled ? rows_per_cta * kBlock : rows_per_cta;
+  return kOffKeys + size_t(key_words(rows)) * 4 + (pooled ? size_t(rows_per_cta) * 4 : 0);
 }
 
 template <bool POOLED>
@@ -326,16 +176,9 @@ __global__ void __launch_bounds__(kThreads, 4) index_select_kernel(const SelectA
   extern __shared__ __align__(1024) uint8_t smem[];
   uint8_t* tiles = smem;
   SelSmall& sm = *reinterpret_cast<SelSmall*>(smem + kOffSmall);
+  uint32_t* s_key = reinterpret_cast<uint32_t*>(smem + kOffKeys);
   const int units_cap = a.rows_per_cta;                                 // rows (flat) or blocks (pooled)
-  const SelLayout lay = sel_layout(units_cap, POOLED);
-  uint32_t* s_key = reinterpret_cast<uint32_t*>(smem + lay.keys);
-  int* s_pool = reinterpret_cast<int*>(smem + lay.pool);
-  uint32_t* s_samp = reinterpret_cast<uint32_t*>(smem + lay.samp);     // [kMaxCluster][kSampleRows]
-  uint32_t* s_hist = reinterpret_cast<uint32_t*>(smem + lay.hist);
-  uint32_t* s_above = reinterpret_cast<uint32_t*>(smem + lay.above);   // row maps of the bracket classes
-  uint32_t* s_inside = reinterpret_cast<uint32_t*>(smem + lay.inside);
-  uint16_t* s_above16 = reinterpret_cast<uint16_t*>(s_above);
-  uint16_t* s_inside16 = reinterpret_cast<uint16_t*>(s_inside);
+  int* s_pool = reinterpret_cast<int*>(s_key + key_words(POOLED ? units_cap * kBlock : units_cap));
 
   const int b = blockIdx.y;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -348,13 +191,7 @@ __global__ void __launch_bounds__(kThreads, 4) index_select_kernel(const SelectA
     }
     mbar_fence_init();
     sm.failed = 0u;
-    sm.br_ok = 0u;
   }
-  // Cluster barrier phase 1 (arrive here, wait before the first remote store):
-  // every CTA of the cluster has started before any CTA writes into another's
-  // shared memory.  Phase 2 (arrive once the sample is pushed, wait when the
-  // bracket is made) publishes the sample.
-  cluster_arrive();
   pdl_wait();   // the pool / n_pool come from the preceding launch
   const int nv = clamp_count(a.n_valid[b], a.valid_cap, a.err);
 
@@ -387,13 +224,7 @@ __global__ void __launch_bounds__(kThreads, 4) index_select_kernel(const SelectA
   const uint8_t* keys = static_cast<const uint8_t*>(a.keys) + (long long)(b / a.seq_div) * a.rows_per_seq * kRowBytes;
   if (warp == kConsumers) {
     int i = 0;
-    bool phase2 = false;
     for (; i < ntiles; ++i) {
-      if (i == kStages) {   // the ring is filled: take part in barrier phases 1 and 2
-        cluster_wait();
-        cluster_arrive();
-        phase2 = true;
-      }
       const int s = i % kStages;
       bool ok = true;
       if (lane == 0 && i >= kStages) ok = mbar_wait(&sm.empty[s], ((i / kStages) - 1) & 1, a.wait_ns);
@@ -427,12 +258,6 @@ __global__ void __launch_bounds__(kThreads, 4) index_select_kernel(const SelectA
       for (int j = max(0, i - kStages); j < i; ++j)
         if (!mbar_wait(&sm.full[j % kStages], (j / kStages) & 1, a.wait_ns)) sm.failed = 1u;
     }
-    __syncwarp();
-    if (!phase2) {
-      cluster_wait();
-      cluster_arrive();
-    }
-    cluster_wait();
   } else {
     const int g = lane >> 2, t = lane & 3;
     const uint4* qp = reinterpret_cast<const uint4*>(static_cast<const uint8_t*>(a.q_idx) +
@@ -442,144 +267,74 @@ __global__ void __launch_bounds__(kThreads, 4) index_select_kernel(const SelectA
     const float w0 = a.w[b * kHeads + 2 * t];
     const float w1 = a.w[b * kHeads + 2 * t + 1];
     const bool relu = a.relu != 0;
-    const float kf = float(a.k);
-    const float nf = float(POOLED ? n_units * kBlock : n_units);   // the query's candidates (an upper bound when pooled)
-    uint32_t* samp_dst = s_samp + crank * kSampleRows;            // this CTA's slice of every CTA's sample
-    bool phase1 = false, phase2 = false, have_br = false, br_ok = false;
-    Bracket br{};
-    br.b_lo = br.b_hi = kBins + 1;
-    // Once the bracket is made: the class maps of this warp's rows of tiles [0, nt).
-    auto classify_done = [&](int nt) {
-      __syncwarp();
-      for (int t0 = 0; t0 < nt; t0 += 2) {
-        const int ti = t0 + (lane >> 4);
-        const int row = ti * kTileRows + warp * 16 + (lane & 15);
-        const uint32_t kk = (ti < nt && row < rows_total) ? s_key[row] : 0u;
-        const uint32_t c = classify(kk, br);
-        const unsigned ma = __ballot_sync(0xffffffffu, c == kAbove);
-        const unsigned mi = __ballot_sync(0xffffffffu, c == kInside);
-        if (lane == 0) {
-          const int h0 = (t0 * kTileRows + warp * 16) >> 4;
-          s_above16[h0] = uint16_t(ma & 0xffffu);
-          s_inside16[h0] = uint16_t(mi & 0xffffu);
-          if (t0 + 1 < nt) {
-            const int h1 = ((t0 + 1) * kTileRows + warp * 16) >> 4;
-            s_above16[h1] = uint16_t(ma >> 16);
-            s_inside16[h1] = uint16_t(mi >> 16);
-          }
-        }
-      }
-    };
-    int i = 0;
-    for (; i < ntiles; ++i) {
-      if (i == kSampleTiles) {   // this warp's sample rows are pushed: barrier phase 2
-        cluster_arrive();
-        phase2 = true;
-      }
-      if (i == kSampleTiles + kBracketLag) {
-        br = make_bracket(s_samp, int(ncta) * kSampleRows, s_hist, sm, kf, nf, tid, lane, warp, &br_ok);
-        classify_done(i);
-        have_br = true;
-      }
+    for (int i = 0; i < ntiles; ++i) {
       const int s = i % kStages;
-      if (!__all_sync(0xffffffffu, mbar_wait(&sm.full[s], (i / kStages) & 1, a.wait_ns))) {
-        if (lane == 0) report(a.err, kErrTimeout, i);
+      if (!mbar_wait(&sm.full[s], (i / kStages) & 1, a.wait_ns)) {
+        report(a.err, kErrTimeout, i);
         sm.failed = 1u;
         break;
       }
-      if (!phase1) {   // every CTA has started: remote stores may begin
-        cluster_wait();
-        phase1 = true;
-      }
       const uint8_t* tile = tiles + s * kTileBytes;
-      uint32_t ra[8], rb[8];
-      {
-        const uint8_t* p = tile + (warp * 16 + g) * kRowBytes + 32 * t;
+      (void)tile;
+      uint32_t ra[kMTiles][8], rb[kMTiles][8];
+#pragma unroll
+      for (int m = 0; m < kMTiles; ++m) {
+        const uint8_t* p = tile + ((warp * kMTiles + m) * 16 + g) * kRowBytes + 32 * t;
         const uint4 x0 = *reinterpret_cast<const uint4*>(p);
         const uint4 x1 = *reinterpret_cast<const uint4*>(p + 16);
         const uint4 y0 = *reinterpret_cast<const uint4*>(p + 8 * kRowBytes);
         const uint4 y1 = *reinterpret_cast<const uint4*>(p + 8 * kRowBytes + 16);
-        ra[0] = x0.x; ra[1] = x0.y; ra[2] = x0.z; ra[3] = x0.w;
-        ra[4] = x1.x; ra[5] = x1.y; ra[6] = x1.z; ra[7] = x1.w;
-        rb[0] = y0.x; rb[1] = y0.y; rb[2] = y0.z; rb[3] = y0.w;
-        rb[4] = y1.x; rb[5] = y1.y; rb[6] = y1.z; rb[7] = y1.w;
+        ra[m][0] = x0.x; ra[m][1] = x0.y; ra[m][2] = x0.z; ra[m][3] = x0.w;
+        ra[m][4] = x1.x; ra[m][5] = x1.y; ra[m][6] = x1.z; ra[m][7] = x1.w;
+        rb[m][0] = y0.x; rb[m][1] = y0.y; rb[m][2] = y0.z; rb[m][3] = y0.w;
+        rb[m][4] = y1.x; rb[m][5] = y1.y; rb[m][6] = y1.z; rb[m][7] = y1.w;
       }
       __syncwarp();
       if (lane == 0) mbar_arrive(&sm.empty[s]);
-      float c0[4] = {0.f, 0.f, 0.f, 0.f}, c1[4] = {0.f, 0.f, 0.f, 0.f};
-      mma_bf16(c0, ra[0], rb[0], ra[1], rb[1], qf[0], qf[1]);
-      mma_bf16(c1, ra[2], rb[2], ra[3], rb[3], qf[2], qf[3]);
-      mma_bf16(c0, ra[4], rb[4], ra[5], rb[5], qf[4], qf[5]);
-      mma_bf16(c1, ra[6], rb[6], ra[7], rb[7], qf[6], qf[7]);
-      float h[4];
 #pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        const float d = c0[e] + c1[e];
-        h[e] = relu ? fmaxf(d, 0.f) : d;
-      }
-      float r0 = __fadd_rn(__fmul_rn(w0, h[0]), __fmul_rn(w1, h[1]));
-      float r1 = __fadd_rn(__fmul_rn(w0, h[2]), __fmul_rn(w1, h[3]));
-      r0 += __shfl_xor_sync(0xffffffffu, r0, 1);
-      r1 += __shfl_xor_sync(0xffffffffu, r1, 1);
-      r0 += __shfl_xor_sync(0xffffffffu, r0, 2);
-      r1 += __shfl_xor_sync(0xffffffffu, r1, 2);
-      const int row = i * kTileRows + warp * 16 + g + 8 * t;   // lanes t < 2 hold rows +0 .. +15
-      uint32_t kk = 0u;                                          // 0: not a candidate
-      if (t < 2 && row < rows_total) {
-        bool valid = true;
-        if (POOLED) {
-          const int blk = s_pool[row / kBlock];
-          valid = blk >= 0 && blk * kBlock + row % kBlock < nv;
+      for (int m = 0; m < kMTiles; ++m) {
+        float c0[4] = {0.f, 0.f, 0.f, 0.f}, c1[4] = {0.f, 0.f, 0.f, 0.f};
+        mma_bf16(c0, ra[m][0], rb[m][0], ra[m][1], rb[m][1], qf[0], qf[1]);
+        mma_bf16(c1, ra[m][2], rb[m][2], ra[m][3], rb[m][3], qf[2], qf[3]);
+        mma_bf16(c0, ra[m][4], rb[m][4], ra[m][5], rb[m][5], qf[4], qf[5]);
+        mma_bf16(c1, ra[m][6], rb[m][6], ra[m][7], rb[m][7], qf[6], qf[7]);
+        float h[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const float d = c0[e] + c1[e];
+          h[e] = relu ? fmaxf(d, 0.f) : d;
         }
-        kk = valid ? score_key(t == 0 ? r0 : r1) : 0u;
-        s_key[row] = kk;
-        if (kk != 0u) {
-          ++my_cnt;
-          my_lo = min(my_lo, kk);
-          my_hi = max(my_hi, kk);
-        }
-      }
-      if (i < kSampleTiles && t < 2)   // the sample: this row's key into every CTA
-        for (int r = 0; r < int(ncta); ++r) dsmem_st_u32(dsmem_addr(samp_dst + row, uint32_t(r)), kk);
-      if (have_br) {
-        const uint32_t c = classify(kk, br);
-        const uint32_t bit = 1u << ((g + 8 * t) & 31);
-        const uint32_t ma = __reduce_or_sync(0xffffffffu, (t < 2 && c == kAbove) ? bit : 0u);
-        const uint32_t mi = __reduce_or_sync(0xffffffffu, (t < 2 && c == kInside) ? bit : 0u);
-        if (lane == 0) {
-          const int hh = (i * kTileRows + warp * 16) >> 4;
-          s_above16[hh] = uint16_t(ma);
-          s_inside16[hh] = uint16_t(mi);
+        float r0 = __fadd_rn(__fmul_rn(w0, h[0]), __fmul_rn(w1, h[1]));
+        float r1 = __fadd_rn(__fmul_rn(w0, h[2]), __fmul_rn(w1, h[3]));
+        r0 += __shfl_xor_sync(0xffffffffu, r0, 1);
+        r1 += __shfl_xor_sync(0xffffffffu, r1, 1);
+        r0 += __shfl_xor_sync(0xffffffffu, r0, 2);
+        r1 += __shfl_xor_sync(0xffffffffu, r1, 2);
+        const int row = i * kTileRows + (warp * kMTiles + m) * 16 + g + 8 * t;
+        if (t < 2 && row < rows_total) {
+          bool valid = true;
+          if (POOLED) {
+            const int blk = s_pool[row / kBlock];
+            valid = blk >= 0 && blk * kBlock + row % kBlock < nv;
+          }
+          const uint32_t kk = valid ? score_key(t == 0 ? r0 : r1) : 0u;   // 0: not a candidate
+          s_key[row] = kk;
+          if (kk != 0u) {
+            ++my_cnt;
+            my_lo = min(my_lo, kk);
+            my_hi = max(my_hi, kk);
+          }
         }
       }
     }
-    if (!phase1) cluster_wait();
-    if (!phase2) {
-      // sample rows this warp did not push (fewer tiles, or a wait gave up): no candidate
-      for (int ti = i; ti < kSampleTiles; ++ti)
-        if (lane < 16)
-          for (int r = 0; r < int(ncta); ++r)
-            dsmem_st_u32(dsmem_addr(samp_dst + ti * kTileRows + warp * 16 + lane, uint32_t(r)), 0u);
-      cluster_arrive();
-    }
-    if (!have_br) {
-      br = make_bracket(s_samp, int(ncta) * kSampleRows, s_hist, sm, kf, nf, tid, lane, warp, &br_ok);
-      classify_done(i);
-    }
-    if (tid == 0) sm.br_ok = br_ok ? 1u : 0u;
   }
   if (tid < 3 && rows_total + tid < key_words(rows_total)) s_key[rows_total + tid] = 0u;   // padding: no candidate
   __syncthreads();   // all keys written; the ring buffer is free for the histogram
-  const int map_n = (rows_total + 31) >> 5;   // class map words in use
   if (sm.failed) {
     // A bounded wait gave up (recorded in the error word): some keys were never
     // written.  This CTA then offers no candidate, so that the cluster's
     // selection stays consistent and every write stays in bounds.
     for (int j = tid; j < key_words(rows_total); j += kThreads) s_key[j] = 0u;
-    for (int j = tid; j < map_n; j += kThreads) {
-      s_above[j] = 0u;
-      s_inside[j] = 0u;
-    }
     my_cnt = 0u;
     my_lo = 0xffffffffu;
     my_hi = 0u;
@@ -611,17 +366,10 @@ __global__ void __launch_bounds__(kThreads, 4) index_select_kernel(const SelectA
   uint32_t fsel = 0u;            // once filtered: the members are also in bin fsel of the last pass
   bool filtered = false, gathered = false, resolved = false;
   uint32_t n_all = 0u;           // valid candidates of the query
-  bool bracket = false;           // the sampled bracket holds the k-th key: its keys were gathered
   for (int step = 0; step < 12 && !resolved; ++step) {
     // (1) count, min and max of the members in every CTA, pushed to every CTA
     {
       uint32_t c = my_cnt, l = my_lo, h = my_hi;   // step 0: tracked while scoring
-      uint32_t na = 0u, ni = 0u;                   // step 0: keys above / inside the bracket
-      if (step == 0)
-        for (int j = tid; j < map_n; j += kThreads) {
-          na += __popc(s_above[j]);
-          ni += __popc(s_inside[j]);
-        }
       if (step > 0) {
         c = 0u;
         l = 0xffffffffu;
@@ -638,34 +386,24 @@ __global__ void __launch_bounds__(kThreads, 4) index_select_kernel(const SelectA
       c = __reduce_add_sync(0xffffffffu, c);
       l = __reduce_min_sync(0xffffffffu, l);
       h = __reduce_max_sync(0xffffffffu, h);
-      na = __reduce_add_sync(0xffffffffu, na);
-      ni = __reduce_add_sync(0xffffffffu, ni);
       if (lane == 0) {
         sm.red[0][warp] = c;
         sm.red[1][warp] = l;
         sm.red[2][warp] = h;
-        sm.red[3][warp] = na;
-        sm.red[4][warp] = ni;
       }
       __syncthreads();
       if (tid < int(ncta)) {
         uint4 v = make_uint4(0u, 0xffffffffu, 0u, 0u);
-        uint4 bv = make_uint4(0u, 0u, sm.br_ok, 0u);
         for (int w = 0; w < kWarpsAll; ++w) {
           v.x += sm.red[0][w];
           v.y = min(v.y, sm.red[1][w]);
           v.z = max(v.z, sm.red[2][w]);
-          bv.x += sm.red[3][w];
-          bv.y += sm.red[4][w];
         }
         dsmem_st_v4u(dsmem_addr(&sm.stats[crank], uint32_t(tid)), v);
-        if (step == 0) dsmem_st_v4u(dsmem_addr(&sm.bstats[crank], uint32_t(tid)), bv);
       }
       cluster_arrive();
-      if (step > 0) {   // region A is written by no other CTA here
-        uint4* hv = reinterpret_cast<uint4*>(histD);
-        for (int j = tid; j < kHistDWords / 4; j += kThreads) hv[j] = make_uint4(0u, 0u, 0u, 0u);
-      }
+      uint4* hv = reinterpret_cast<uint4*>(histD);   // region A is written by no other CTA here
+      for (int j = tid; j < kHistDWords / 4; j += kThreads) hv[j] = make_uint4(0u, 0u, 0u, 0u);
       __syncthreads();
       cluster_wait();
     }
@@ -686,39 +424,6 @@ __global__ void __launch_bounds__(kThreads, 4) index_select_kernel(const SelectA
       }
       resolved = true;
       break;
-    }
-    if (step == 0) {
-      // The sampled bracket holds the k-th key when fewer than k keys lie above
-      // it and at least k at or above its low end; its keys, few enough to
-      // gather, then decide the threshold.  Otherwise the radix passes below run.
-      uint32_t n_above = 0u, n_in = 0u, padded = 0u;
-      bool usable = true;
-      for (int r = 0; r < int(ncta); ++r) {
-        const uint4 v = sm.bstats[r];
-        n_above += v.x;
-        n_in += v.y;
-        padded += (v.y + 3u) & ~3u;
-        usable = usable && v.z != 0u;
-      }
-      if (usable && n_above < k && k <= n_above + n_in && padded <= uint32_t(kGatherWords)) {
-        if (tid < int(ncta)) {
-          sm.above_r[tid] = sm.bstats[tid].x;
-          sm.cnt_r[tid] = sm.bstats[tid].y;
-        }
-        __syncthreads();
-        need = k - n_above;
-        lo = 1u;            // the gathered keys are exactly the members
-        hi = 0xffffffffu;
-        bracket = true;
-        gathered = true;
-        resolved = true;
-        break;
-      }
-      // The histogram's region A is zeroed only now at step 0: with the bracket,
-      // peers push their gathered keys into it right after the barrier above.
-      uint4* hv = reinterpret_cast<uint4*>(histD);
-      for (int j = tid; j < kHistDWords / 4; j += kThreads) hv[j] = make_uint4(0u, 0u, 0u, 0u);
-      __syncthreads();
     }
     lo = glo;   // the members are exactly the keys in [lo, hi] (bins are contiguous key ranges)
     hi = ghi;
@@ -853,21 +558,9 @@ __global__ void __launch_bounds__(kThreads, 4) index_select_kernel(const SelectA
       G += (sm.cnt_r[r] + 3u) & ~3u;
     }
     const uint32_t my_in = sm.cnt_r[crank];
-    if (bracket) {
-      // members: the keys inside the bracket, from its row map
-      for (int w = tid; w < map_n; w += kThreads) {
-        uint32_t m = s_inside[w];
-        while (m != 0u) {
-          const int j = w * 32 + __ffs(m) - 1;
-          m &= m - 1u;
-          const uint32_t p = atomicAdd(&sm.gcount, 1u);
-          if (p < my_in) gk[my_off + p] = s_key[j];
-        }
-      }
-    }
-    // otherwise members: keys in [lo, hi] whose bin byte is fsel; 16 bytes compared per read
+    // members: keys in [lo, hi] whose bin byte is fsel; 16 bytes compared per read
     const uint32_t sel4 = fsel * 0x01010101u;
-    const int nbv = bracket ? 0 : (nvec + 3) >> 2;
+    const int nbv = (nvec + 3) >> 2;
     for (int v = tid; v < nbv; v += kThreads) {   // few keys match: one atomic each
       const uint4 w4 = reinterpret_cast<const uint4*>(kbin)[v];
       const uint32_t w[4] = {w4.x, w4.y, w4.z, w4.w};
@@ -1081,71 +774,6 @@ __global__ void __launch_bounds__(kThreads, 4) index_select_kernel(const SelectA
       eqb += sm.eq_r[r];
     }
   }
-  int* out = a.out + (long long)b * a.ld_out;
-  if (bracket) {
-    // The selected rows are the keys above the bracket, the bracket's keys
-    // above T, and its first `quota` keys at T in row order.  Warp 0 walks the
-    // row maps (4 words of 32 rows per lane, in row order): scans of the tie
-    // and selection counts give each lane its ties to take and its first slot.
-    if (warp == 0) {
-      uint32_t selw[4], eqw[4], neq = 0u;
-#pragma unroll
-      for (int u = 0; u < 4; ++u) {
-        const int w = lane * 4 + u;
-        uint32_t sw = 0u, ew = 0u;
-        if (w < map_n) {
-          sw = s_above[w];
-          uint32_t m = s_inside[w];
-          while (m != 0u) {
-            const int bit = __ffs(m) - 1;
-            m &= m - 1u;
-            const uint32_t kk = s_key[w * 32 + bit];
-            if (kk > T)
-              sw |= 1u << bit;
-            else if (kk == T && q > 0u)
-              ew |= 1u << bit;
-          }
-        }
-        selw[u] = sw;
-        eqw[u] = ew;
-        neq += uint32_t(__popc(ew));
-      }
-      uint32_t incl = neq;
-#pragma unroll
-      for (int o = 1; o < 32; o <<= 1) {
-        const uint32_t y = __shfl_up_sync(0xffffffffu, incl, o);
-        if (lane >= o) incl += y;
-      }
-      uint32_t eqb = incl - neq, nsel = 0u;
-#pragma unroll
-      for (int u = 0; u < 4; ++u) {
-        uint32_t ew = eqw[u];
-        while (ew != 0u && eqb < quota) {
-          const int bit = __ffs(ew) - 1;
-          ew &= ew - 1u;
-          selw[u] |= 1u << bit;
-          ++eqb;
-        }
-        nsel += uint32_t(__popc(selw[u]));
-      }
-      incl = nsel;
-#pragma unroll
-      for (int o = 1; o < 32; o <<= 1) {
-        const uint32_t y = __shfl_up_sync(0xffffffffu, incl, o);
-        if (lane >= o) incl += y;
-      }
-      uint32_t slot = offset + incl - nsel;
-#pragma unroll
-      for (int u = 0; u < 4; ++u) {
-        uint32_t sw = selw[u];
-        while (sw != 0u) {
-          const int j = (lane * 4 + u) * 32 + __ffs(sw) - 1;
-          sw &= sw - 1u;
-          out[slot++] = POOLED ? s_pool[j / kBlock] * kBlock + j % kBlock : begin + j;
-        }
-      }
-    }
-  } else {
   // Each warp owns a contiguous run of positions.  One pass lists, in order, the
   // positions of the run's keys above or at the threshold (flagged) in the run's
   // own stretch of a stage buffer (the ring is free now); the warps' counts give
@@ -1177,6 +805,7 @@ __global__ void __launch_bounds__(kThreads, 4) index_select_kernel(const SelectA
     eq_before += sm.red[1][w];
   }
   uint32_t slot = offset + gt_before + min(eq_before, quota);
+  int* out = a.out + (long long)b * a.ld_out;
   for (uint32_t i0 = 0; i0 < wn; i0 += 32) {
     const uint32_t i = i0 + uint32_t(lane);
     const uint32_t v = i < wn ? stage[p0 + i] : 0u;
@@ -1196,13 +825,7 @@ __global__ void __launch_bounds__(kThreads, 4) index_select_kernel(const SelectA
     slot += uint32_t(__popc(mt));
     eq_before += uint32_t(__popc(me));
   }
-  }
   const int selected = int(min(n_all, k));
-  // diagnostics counters in the error word's header: selections run, and those the bracket did not settle
-  if (a.err != nullptr && crank == 0 && tid == 0 && n_all > k) {
-    atomicAdd(a.err + kCounterSelections, 1);
-    if (!bracket) atomicAdd(a.err + kCounterFallbacks, 1);
-  }
   if (crank == 0) {
     if (a.n_out != nullptr && tid == 0) a.n_out[b] = selected;
     for (int j = selected + tid; j < a.k; j += kThreads) out[j] = -1;

@@ -11,11 +11,6 @@ constexpr int kErrBadIndex = 1;   // a main-KV index outside [0, n_entries)
 constexpr int kErrBadCount = 2;   // n_valid / n_swa / n_pool / n_cand outside its range
 constexpr int kErrTimeout = 4;    // a bounded wait on an mbarrier gave up
 constexpr int kErrBadPool = 8;    // a pooled block id outside [0, ceil(n_valid / block))
-// Diagnostic counters in the workspace header (words 4 and 5): fused
-// selections that had more candidates than k, and those of them that the
-// sampled bracket did not settle (the radix passes ran instead).
-constexpr int kCounterSelections = 4;
-constexpr int kCounterFallbacks = 5;
 
 // Indexer scoring: s = sum_h w_h * ReLU(q_h . k) over a flat row range or the
 // entries of pooled blocks.

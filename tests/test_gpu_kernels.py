@@ -381,57 +381,6 @@ def test_index_topk_pooled_wide_or_negative_scores(csa2, case):
     assert_no_device_error(csa2, ws)
 
 
-@pytest.mark.parametrize("order", ["random", "ascending"])
-def test_index_topk_fused_sampled_bracket_and_its_fallback(csa2, order):
-    """The fused selection first tries a key bracket estimated from a sample (each CTA's
-    first two tiles) and falls back to its exact radix passes when the bracket misses.
-    Random integer data (the 128K Reindex workload's block and pooled stages at batch 8):
-    every selection is settled by the bracket.  Scores ascending with the index (one-hot
-    queries, a 200-level ramp): the sample sits at the low end of each CTA's range, the
-    bracket misses and every selection takes the fallback.  Both match the oracle."""
-    B = 8
-    if order == "random":
-        wl = W.named("reindex_b64_128k", batch=B)
-        d = csa2.upload(wl)
-        sh = wl.shape
-        csa2.block_keys(sh, d["k_idx"], d["n_valid"], d["kb"], d["ws"], round_to_int=True)
-        csa2.debug_select_counters(d["ws"])
-        csa2.layer_group(sh, d["layers"], d["k_main"], d["v_main"], d["k_idx"], d["kb"], d["n_valid"], d["n_swa"],
-                         d["ws"])
-        sel, fb = csa2.debug_select_counters(d["ws"])
-        ref = oracle.run_group(wl, want_attention=False)
-        assert np.array_equal(d["layers"][0]["idx_out"].cpu().numpy(), ref[0]["idx"])
-        assert sel == 2 * B, sel                          # the block stage and the pooled stage of every query
-        assert fb == 0, f"{fb} of {sel} selections fell back"
-        assert_no_device_error(csa2, d["ws"])
-        return
-    N, K = 32768, 512
-    sh = _shape(batch=B, n_entries=N, topk=K, pool_blocks=0)
-    rng = np.random.default_rng(5)
-    k_f = np.zeros((B, N, sh.idx_dim), dtype=np.float32)
-    k_f[:, :, 0] = np.floor(np.arange(N) * 200.0 / N)[None, :]
-    k_f[:, :, 1:] = rng.integers(-4, 5, size=(B, N, sh.idx_dim - 1))     # ignored by the one-hot queries
-    k_idx = W.f32_to_bf16_bits(k_f)
-    q_f = np.zeros((B, sh.idx_heads, sh.idx_dim), dtype=np.float32)
-    q_f[:, :, 0] = 1.0
-    q_idx = W.f32_to_bf16_bits(q_f)
-    w = np.ones((B, sh.idx_heads), dtype=np.float32)
-    n_valid = np.full(B, N, dtype=np.int32)
-    n_valid[1] = N - 1000
-    ws = csa2.workspace(sh)
-    csa2.debug_select_counters(ws)
-    idx = torch.full((B, K), -9, dtype=torch.int32, device="cuda")
-    csa2.index_topk(sh, bf16(q_idx), f32(w), bf16(k_idx), i32(n_valid), K, idx, ws)
-    sel, fb = csa2.debug_select_counters(ws)
-    assert sel == B and fb == B, (sel, fb)
-    got = idx.cpu().numpy()
-    for b in range(B):
-        r = oracle.layer_indices(oracle.to_f64(q_idx[b]), w[b].astype(np.float64), oracle.to_f64(k_idx[b]), None,
-                                 int(n_valid[b]), topk=K, block=8, pool=0, hier=False)
-        assert got[b].tolist() == r["idx"].tolist(), f"ascending query {b}"
-    assert_no_device_error(csa2, ws)
-
-
 # ------------------------------------------------------------------ bounded device waits
 
 def test_bounded_wait_gives_up_and_reports_timeout(csa2):
