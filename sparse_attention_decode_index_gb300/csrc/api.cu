@@ -48,7 +48,7 @@ int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
 
 struct WsLayout {
   size_t hdr, pool, n_pool, n_blk, blk_scores, tok_scores, tok_cand, n_cand, tk_ids_a, tk_sc_a, tk_ids_b,
-      tk_sc_b, idx, attn_part, total;
+      tk_sc_b, idx, total;
   int64_t nb_cap, tok_ld, tk_chunks, tk_kmax;
 };
 
@@ -85,9 +85,6 @@ WsLayout layout(const csa2_shape& s) {
   L.tk_ids_b = take(tk);
   L.tk_sc_b = take(tk);
   L.idx = take(size_t(B) * s.topk * 4);
-  // fast attention: every CTA of a query's cluster leaves its partial O of all heads here
-  const int64_t attn_c = attn_fast(s) ? attn_cluster(s.topk, s.swa) : 0;
-  L.attn_part = take(size_t(B * attn_c * s.q_heads * s.v_dim) * 4);
   L.total = off;
   return L;
 }
@@ -260,7 +257,7 @@ int do_topk(const csa2_shape& s, const WsLayout& L, void* ws, const float* score
 
 int do_attn(const csa2_shape& s, const void* q, const void* k_main, const void* v_main, const int32_t* idx,
             const void* k_swa, const void* v_swa, const int32_t* n_swa, float* out, float* lse, int* err,
-            float* part, cudaStream_t st, bool swa_only = false, bool release_at_end = false) {
+            cudaStream_t st, bool swa_only = false, bool release_at_end = false) {
   AttnArgs a{};
   a.release_at_end = release_at_end ? 1 : 0;
   a.q = q;
@@ -281,7 +278,6 @@ int do_attn(const csa2_shape& s, const void* q, const void* k_main, const void* 
   a.v_dim = s.v_dim;
   a.dtype = s.dtype;
   a.scale = softmax_scale(s);
-  a.part = part;
   a.err = err;
   return cuda_status(launch_attn(a, attn_fast(s), s.batch, st));
 }
@@ -543,8 +539,7 @@ int csa2_sparse_attn(const csa2_shape* shape, const void* q, const void* k_main,
   CSA2_TRY(check_attn_args(s, q, k_main, v_main, out));
   CSA2_TRY(check_sswa(s, k_swa, v_swa, n_swa));
   const WsLayout L = layout(s);
-  return do_attn(s, q, k_main, v_main, idx, k_swa, v_swa, n_swa, out, lse, at<int>(ws, L.hdr),
-                 at<float>(ws, L.attn_part), stream);
+  return do_attn(s, q, k_main, v_main, idx, k_swa, v_swa, n_swa, out, lse, at<int>(ws, L.hdr), stream);
 }
 
 int csa2_layer_group(const csa2_shape* shape, const csa2_layer* layers, int32_t n_layers, const void* k_main,
@@ -587,8 +582,8 @@ int csa2_layer_group(const csa2_shape* shape, const csa2_layer* layers, int32_t 
     // another attention-only launch next (Reuse or SWA layer): release it at this attention's end
     const bool attn_next = l + 1 < n_layers && (layers[l + 1].mode == CSA2_REUSE || layers[l + 1].mode == CSA2_SWA);
     if (y.mode == CSA2_SWA) {
-      CSA2_TRY(do_attn(s, y.q, k_main, v_main, nullptr, y.k_swa, y.v_swa, n_swa, y.out, y.lse, err,
-                     at<float>(ws, L.attn_part), stream, true, attn_next));
+      CSA2_TRY(do_attn(s, y.q, k_main, v_main, nullptr, y.k_swa, y.v_swa, n_swa, y.out, y.lse, err, stream, true,
+                       attn_next));
       continue;
     }
     if (y.mode != CSA2_REUSE) {
@@ -626,8 +621,8 @@ int csa2_layer_group(const csa2_shape* shape, const csa2_layer* layers, int32_t 
       }
       cur = dst;
     }
-    CSA2_TRY(do_attn(s, y.q, k_main, v_main, cur, y.k_swa, y.v_swa, n_swa, y.out, y.lse, err,
-                     at<float>(ws, L.attn_part), stream, false, attn_next));
+    CSA2_TRY(do_attn(s, y.q, k_main, v_main, cur, y.k_swa, y.v_swa, n_swa, y.out, y.lse, err, stream, false,
+                     attn_next));
   }
   return CSA2_OK;
 }

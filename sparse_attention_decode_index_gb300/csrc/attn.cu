@@ -56,6 +56,8 @@ constexpr int kOffL = kOffM + kMaxCluster * kH * 4;   // [kMaxCluster][kH] l of 
 constexpr int kOffValid = kOffL + kMaxCluster * kH * 4;
 constexpr int kSmemBytes = kOffValid + kSlots * 4;
 constexpr int kHalf = kSlots / 2;                 // slots per gather barrier (80)
+constexpr int kPRow = kDv + 8;                    // partial O row (fp32): padded against bank conflicts
+static_assert(kH * kPRow * 4 + kMaxCluster * kH * 4 <= kSlots * kKRow, "partials and weights fit the K region");
 static_assert(kSlots % 16 == 0, "PV k-steps need 16-key groups");
 static_assert(kNT % 4 == 0, "each gather half covers whole n-tile pairs");
 
@@ -258,11 +260,13 @@ __global__ void __launch_bounds__(kThreads, 2) attn_mma_kernel(const AttnArgs a)
     }
   }
 
-  // --- merge across the cluster, one barrier: every CTA pushes the (m, l) of
-  // its rows into the table of the CTA that owns those heads and writes its
-  // unscaled partial O of all heads to global scratch (L2); after the barrier
-  // the owner weights the partials by exp2(m_c - M) and sums them in fixed
-  // CTA order.
+  // --- merge across the cluster: every CTA pushes the (m, l) of its rows into
+  // the table of the CTA that owns those heads and leaves its unscaled partial
+  // O of all heads in its own shared memory (the K region, free once every
+  // warp is done with the keys and values); after one cluster barrier the
+  // owner weights the partials by exp2(m_c - M) / L and sums them in fixed CTA
+  // order, reading its peers' partials through distributed shared memory.  A
+  // second (split) barrier keeps every CTA resident until its partials are read.
   const int h0 = warp * 16 + g, h1 = h0 + 8;
   const int per_owner = (kH + int(ncta) - 1) / int(ncta);
   if (t == 0) {
@@ -272,25 +276,17 @@ __global__ void __launch_bounds__(kThreads, 2) attn_mma_kernel(const AttnArgs a)
     dsmem_st_f32(dsmem_addr(sM + crank * kH + h1, own1), m1);
     dsmem_st_f32(dsmem_addr(sL + crank * kH + h1, own1), l1);
   }
-  {
-    // Lane pairs (t, t ^ 1) trade halves so that the even lane stores 4
-    // consecutive columns of row h0 and the odd lane 4 of row h1.
-    const bool even = (t & 1) == 0;
-    float* prow = a.part + ((size_t)(b * int(ncta) + int(crank)) * kH + (even ? h0 : h1)) * kDv;
+  __syncthreads();   // every warp is done with the K and V rows
+  float* sP = reinterpret_cast<float*>(sK);   // [kH][kPRow] this CTA's unscaled partial O
 #pragma unroll
-    for (int j = 0; j < kDv / 8; ++j) {
-      const float rx = __shfl_xor_sync(0xffffffffu, even ? o[j][2] : o[j][0], 1);
-      const float ry = __shfl_xor_sync(0xffffffffu, even ? o[j][3] : o[j][1], 1);
-      const int col = 8 * j + 2 * t - (even ? 0 : 2);
-      __stcg(reinterpret_cast<float4*>(prow + col),
-             even ? make_float4(o[j][0], o[j][1], rx, ry) : make_float4(rx, ry, o[j][2], o[j][3]));
-    }
+  for (int j = 0; j < kDv / 8; ++j) {
+    *reinterpret_cast<float2*>(sP + h0 * kPRow + 8 * j + 2 * t) = make_float2(o[j][0], o[j][1]);
+    *reinterpret_cast<float2*>(sP + h1 * kPRow + 8 * j + 2 * t) = make_float2(o[j][2], o[j][3]);
   }
   cluster_sync_all();   // tables and partials of every CTA are complete and visible
-  // the owner sums its heads in CTA order (L2 loads: the partials come from other SMs);
-  // weights exp2(m_r - M) / L per (CTA, head) first, into the now unused K region
+  // the owner's weights exp2(m_r - M) / L per (CTA, head) first, after the partials
   const int hb = int(crank) * per_owner, he = min(kH, hb + per_owner);
-  float* sW = reinterpret_cast<float*>(sK);   // [kMaxCluster][kH]
+  float* sW = sP + kH * kPRow;   // [kMaxCluster][kH]
   for (int h = hb + tid; h < he; h += kThreads) {
     float M = -INFINITY;
     for (uint32_t r = 0; r < ncta; ++r) M = fmaxf(M, sM[r * kH + h]);
@@ -305,8 +301,8 @@ __global__ void __launch_bounds__(kThreads, 2) attn_mma_kernel(const AttnArgs a)
     for (uint32_t r = 0; r < ncta; ++r) sW[r * kH + h] *= inv;
   }
   __syncthreads();
-  // Up to kItems (head, 4 columns) items per thread, all their partial loads issued
-  // before any is used (each item reads one float4 from every CTA of the cluster).
+  // Up to kItems (head, 4 columns) items per thread, every partial load of them
+  // issued before any is used (each item reads one float4 from every CTA).
   constexpr int kItems = 4;
   const int n_items = (he - hb) * (kDv / 4);
   for (int e0 = tid; e0 < n_items; e0 += kItems * kThreads) {
@@ -317,9 +313,7 @@ __global__ void __launch_bounds__(kThreads, 2) attn_mma_kernel(const AttnArgs a)
       const int h = hb + e / (kDv / 4), d4 = e % (kDv / 4);
 #pragma unroll
       for (int r = 0; r < kMaxCluster; ++r)
-        if (e < n_items && r < int(ncta))
-          v[m][r] = __ldcg(reinterpret_cast<const float4*>(a.part + ((size_t)(b * int(ncta) + r) * kH + h) * kDv +
-                                                           4 * d4));
+        if (e < n_items && r < int(ncta)) v[m][r] = dsmem_ld_v4f(dsmem_addr(sP + h * kPRow + 4 * d4, uint32_t(r)));
     }
 #pragma unroll
     for (int m = 0; m < kItems; ++m) {
@@ -338,22 +332,8 @@ __global__ void __launch_bounds__(kThreads, 2) attn_mma_kernel(const AttnArgs a)
         }
       *reinterpret_cast<float4*>(a.out + ((long long)b * kH + h) * kDv + 4 * d4) = acc;
     }
-    // The partials just combined are dead (every launch writes them before it
-    // reads them): drop their L2 lines instead of letting them be written back
-    // to HBM during the next launches' streams.  The 8 lanes 8g .. 8g + 7 read
-    // one 128-byte line of each CTA's partial row; lane 8g + r drops CTA r's.
-    __syncwarp();
-#pragma unroll
-    for (int m = 0; m < kItems; ++m) {
-      const int e = e0 + m * kThreads;
-      const int r = lane & 7;
-      if (e < n_items && r < int(ncta)) {
-        const int h = hb + e / (kDv / 4), d4 = (e % (kDv / 4)) & ~7;
-        const float* line = a.part + ((size_t)(b * int(ncta) + r) * kH + h) * kDv + 4 * d4;
-        asm volatile("discard.global.L2 [%0], 128;" ::"l"(line) : "memory");
-      }
-    }
   }
+  cluster_arrive();   // this CTA has read its peers' partials
   if (a.lse != nullptr && tid < he - hb) {
     const int h = hb + tid;
     float M = -INFINITY;
@@ -363,6 +343,7 @@ __global__ void __launch_bounds__(kThreads, 2) attn_mma_kernel(const AttnArgs a)
       if (sM[r * kH + h] != -INFINITY) L += exp2f(sM[r * kH + h] - M) * sL[r * kH + h];
     a.lse[(long long)b * kH + h] = M == -INFINITY ? -INFINITY : (M + log2f(L)) * 0.6931471805599453f;
   }
+  cluster_wait();     // every peer has read this CTA's partials: its shared memory may be released
   // Before another attention launch (a Reuse or SWA layer next), its CTAs are
   // let in only now: placed early, they slowed this launch's last clusters
   // (encoder stack Full + 5 Reuse: 321 -> 293 us per group step).

@@ -208,6 +208,15 @@ CSA2_DEV float dsmem_ld_f32(uint32_t addr) {
   return v;
 }
 
+CSA2_DEV float4 dsmem_ld_v4f(uint32_t addr) {
+  float4 v;
+  asm volatile("ld.shared::cluster.v4.f32 {%0, %1, %2, %3}, [%4];"
+               : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
+               : "r"(addr)
+               : "memory");
+  return v;
+}
+
 // ------------------------------------------------------------------ element access
 
 CSA2_DEV float load_elem(const void* base, long long i, int dtype) {

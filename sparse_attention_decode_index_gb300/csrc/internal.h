@@ -66,7 +66,6 @@ struct AttnArgs {
   int n_entries, topk, swa;
   int heads, k_dim, v_dim, dtype;
   float scale;               // softmax scale (natural-log domain)
-  float* part;               // fast path: [B, cluster, H, dv] fp32 partials (workspace scratch)
   int* err;
   int release_at_end;        // fast path: let the next launch place its CTAs only at this one's end
 };
