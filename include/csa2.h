@@ -304,6 +304,54 @@ int csa2_layer_group_static(const csa2_shape* shape, const csa2_layer* layers, i
  * The paper has no counterpart. */
 int csa2_read_static_device_error(csa2_stream_t stream, int32_t* detail);
 
+/* ---------------------------------------------------------------- context parallelism
+ * One long sequence per query split over G ranks by block-aligned entry
+ * ranges: rank g holds entries [e0_g, e0_g + n_loc_g) of every sequence.  The
+ * pages describe no multi-GPU scheme; the split keeps the method's results
+ * because its selection order (score descending, id ascending) is a strict
+ * total order -- the Top-k of a union is the Top-k of the union of the parts'
+ * Top-k lists -- and softmax partials over disjoint key sets combine exactly by
+ * their log-sum-exp.  It serves contexts beyond one GPU, which the
+ * architecture page's bullet "Hierarchical indexer" (at most 16,384
+ * candidates whatever the context length) makes cheap to select over.  The
+ * ranks exchange (score, id) lists and (out, lse) partials with their own
+ * collectives; these calls are the per-rank steps around the exchanges. */
+
+/* Keep the ids of each row that fall in [lo, hi), in their order, add delta,
+ * and write them compacted to out[b, 0 .. n) with -1 after (n_out[b] = n).
+ * Used both ways: a rank's local ids to global (lo = 0, hi = n_loc,
+ * delta = e0) and a global list to a rank's local ids (lo = e0,
+ * hi = e0 + n_loc, delta = -e0).  ids < 0 are dropped.  When a row keeps more
+ * than ld_out ids the rest are dropped and the device error word records a
+ * bad count.
+ *   ids [batch, ld]   out [batch, ld_out]   n_out [batch] (nullable)
+ *   ws: only its 256-byte header (error word) is used. */
+int csa2_shard_slice(const int32_t* ids, int32_t batch, int32_t ld, int32_t lo, int32_t hi, int32_t delta,
+                     int32_t* out, int32_t ld_out, int32_t* n_out, void* ws, size_t ws_bytes, csa2_stream_t stream);
+
+/* A rank's valid entries (div = 1) or valid blocks (div = block) per query:
+ * out[b] = ceil(clamp(n_valid[b] - e0, 0, n_loc) / div).
+ *   n_valid [batch] (global counts)   out [batch] */
+int csa2_shard_counts(const int32_t* n_valid, int32_t batch, int32_t e0, int32_t n_loc, int32_t div, int32_t* out,
+                      csa2_stream_t stream);
+
+/* The G parts' (id, score) lists of every row side by side, in part order:
+ * ids_out[b, g*k + p] = ids[g, b, p] and likewise for the scores (nullable),
+ * turning the [parts, batch, k] result of an all-gather into the [batch,
+ * parts*k] candidate rows of csa2_topk. */
+int csa2_concat_parts(int32_t parts, int32_t batch, int32_t k, const int32_t* ids, const float* scores,
+                      int32_t* ids_out, float* scores_out, csa2_stream_t stream);
+
+/* Combine the softmax attention of `parts` disjoint key sets, in part order:
+ * with M = max_g lse_g and w_g = exp(lse_g - M),
+ *   out = sum_g w_g out_g / sum_g w_g,   lse = M + log(sum_g w_g);
+ * parts with lse = -inf (no key) contribute nothing; all -inf gives out = 0
+ * and lse = -inf.  Rows are (query, head) pairs.
+ *   out_parts [parts, rows, v_dim]  lse_parts [parts, rows] (natural log)
+ *   out [rows, v_dim]  lse [rows] (nullable) */
+int csa2_merge_attn(int32_t parts, int32_t rows, int32_t v_dim, const float* out_parts, const float* lse_parts,
+                    float* out, float* lse, csa2_stream_t stream);
+
 /* Static description of a status code. */
 const char* csa2_status_str(int status);
 

@@ -18,7 +18,7 @@ ROOT = os.path.dirname(HERE)
 CSRC = os.path.join(HERE, "csrc")
 BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(HERE, "libcsa2.so")
-SOURCES = ["api.cu", "indexer.cu", "topk.cu", "attn.cu", "fused.cu", "static_ws.cu", "append.cu"]
+SOURCES = ["api.cu", "indexer.cu", "topk.cu", "attn.cu", "fused.cu", "static_ws.cu", "append.cu", "shard.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

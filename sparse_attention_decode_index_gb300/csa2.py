@@ -72,6 +72,10 @@ _SIGS = {
     "csa2_layer_group_static": (ctypes.c_int, [ctypes.POINTER(CShape), ctypes.POINTER(CLayer), _I32, _VP, _VP,
                                                _VP, _VP, _VP, _VP, _VP]),
     "csa2_read_static_device_error": (ctypes.c_int, [_VP, ctypes.POINTER(_I32)]),
+    "csa2_shard_slice": (ctypes.c_int, [_VP, _I32, _I32, _I32, _I32, _I32, _VP, _I32, _VP, _VP, _SZ, _VP]),
+    "csa2_shard_counts": (ctypes.c_int, [_VP, _I32, _I32, _I32, _I32, _VP, _VP]),
+    "csa2_concat_parts": (ctypes.c_int, [_I32, _I32, _I32, _VP, _VP, _VP, _VP, _VP]),
+    "csa2_merge_attn": (ctypes.c_int, [_I32, _I32, _I32, _VP, _VP, _VP, _VP, _VP]),
     "csa2_debug_wait_timeout": (ctypes.c_int, [ctypes.POINTER(CShape), _VP, _VP, _VP, _VP, _I32, _VP, ctypes.c_uint32,
                                                _VP, _SZ, _VP]),
 }
@@ -333,6 +337,37 @@ def read_static_device_error(stream=None):
     d = _I32(0)
     st = lib().csa2_read_static_device_error(_stream(stream), ctypes.byref(d))
     return int(st), int(d.value)
+
+
+def shard_slice(ids, lo: int, hi: int, delta: int, out, ws, n_out=None, stream=None):
+    """Keep each row's ids in [lo, hi), shifted by delta, compacted into out (-1 padded)."""
+    _check(lib().csa2_shard_slice(_ptr(ids, torch.int32, "ids"), int(ids.shape[0]), int(ids.shape[1]), int(lo),
+                                  int(hi), int(delta), _ptr(out, torch.int32, "out"), int(out.shape[1]),
+                                  _ptr(n_out, torch.int32, "n_out"), *_ws(ws), _stream(stream)), "csa2_shard_slice")
+
+
+def shard_counts(n_valid, e0: int, n_loc: int, out, div: int = 1, stream=None):
+    """A rank's valid entries (div 1) or blocks (div = block): ceil(clamp(n_valid - e0, 0, n_loc) / div)."""
+    _check(lib().csa2_shard_counts(_ptr(n_valid, torch.int32, "n_valid"), int(n_valid.shape[0]), int(e0), int(n_loc),
+                                   int(div), _ptr(out, torch.int32, "out"), _stream(stream)), "csa2_shard_counts")
+
+
+def concat_parts(ids, scores, ids_out, scores_out, stream=None):
+    """[parts, batch, k] lists side by side into [batch, parts * k] rows (scores may be None)."""
+    parts, batch, k = (int(x) for x in ids.shape)
+    _check(lib().csa2_concat_parts(parts, batch, k, _ptr(ids, torch.int32, "ids"), _ptr(scores, torch.float32, "scores"),
+                                   _ptr(ids_out, torch.int32, "ids_out"), _ptr(scores_out, torch.float32, "scores_out"),
+                                   _stream(stream)), "csa2_concat_parts")
+
+
+def merge_attn(out_parts, lse_parts, out, lse=None, stream=None):
+    """Combine softmax partials [parts, ..., v_dim] / [parts, ...] in part order into out / lse."""
+    parts = int(out_parts.shape[0])
+    v_dim = int(out_parts.shape[-1])
+    rows = int(lse_parts[0].numel())
+    _check(lib().csa2_merge_attn(parts, rows, v_dim, _ptr(out_parts, torch.float32, "out_parts"),
+                                 _ptr(lse_parts, torch.float32, "lse_parts"), _ptr(out, torch.float32, "out"),
+                                 _ptr(lse, torch.float32, "lse"), _stream(stream)), "csa2_merge_attn")
 
 
 def debug_wait_timeout(shape, q_idx, w, k_idx, n_valid, k: int, idx_out, wait_limit_ns: int, ws, stream=None):

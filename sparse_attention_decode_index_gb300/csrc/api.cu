@@ -7,6 +7,7 @@
 // with its own indexer query), Reuse layers attend with the latest indices,
 // and every layer attends with its own query and SWA KV.
 #include <atomic>
+#include <climits>
 #include <cstdint>
 #include <cstring>
 #include <mutex>
@@ -625,6 +626,63 @@ int csa2_layer_group(const csa2_shape* shape, const csa2_layer* layers, int32_t 
                      attn_next));
   }
   return CSA2_OK;
+}
+
+int csa2_shard_slice(const int32_t* ids, int32_t batch, int32_t ld, int32_t lo, int32_t hi, int32_t delta,
+                     int32_t* out, int32_t ld_out, int32_t* n_out, void* ws, size_t ws_bytes, csa2_stream_t stream) {
+  if (ids == nullptr || out == nullptr || batch < 1 || ld < 1 || ld_out < 1 || lo > hi) return CSA2_ERR_INVALID_ARG;
+  if (ld > (1 << 24) || ld_out > (1 << 24) || batch > (1 << 20)) return CSA2_ERR_UNSUPPORTED;
+  if (int64_t(hi) + delta > INT32_MAX || int64_t(lo) + delta < INT32_MIN) return CSA2_ERR_INVALID_ARG;
+  if (ws == nullptr || ws_bytes < 256 || (reinterpret_cast<uintptr_t>(ws) & (kAlign - 1)) != 0) return CSA2_ERR_WORKSPACE;
+  ShardSliceArgs a{};
+  a.ids = ids;
+  a.ld = ld;
+  a.lo = lo;
+  a.hi = hi;
+  a.delta = delta;
+  a.out = out;
+  a.ld_out = ld_out;
+  a.n_out = n_out;
+  a.err = static_cast<int*>(ws);
+  return cuda_status(launch_shard_slice(a, batch, stream));
+}
+
+int csa2_shard_counts(const int32_t* n_valid, int32_t batch, int32_t e0, int32_t n_loc, int32_t div, int32_t* out,
+                      csa2_stream_t stream) {
+  if (n_valid == nullptr || out == nullptr || batch < 1 || e0 < 0 || n_loc < 0 || div < 1) return CSA2_ERR_INVALID_ARG;
+  return cuda_status(launch_shard_counts(n_valid, batch, e0, n_loc, div, out, stream));
+}
+
+int csa2_concat_parts(int32_t parts, int32_t batch, int32_t k, const int32_t* ids, const float* scores,
+                      int32_t* ids_out, float* scores_out, csa2_stream_t stream) {
+  if (parts < 1 || batch < 1 || k < 1 || ids == nullptr || ids_out == nullptr) return CSA2_ERR_INVALID_ARG;
+  if (scores != nullptr && scores_out == nullptr) return CSA2_ERR_INVALID_ARG;
+  if (int64_t(parts) * k > (1 << 28)) return CSA2_ERR_UNSUPPORTED;
+  ConcatArgs a{};
+  a.ids = ids;
+  a.scores = scores;
+  a.ids_out = ids_out;
+  a.scores_out = scores_out;
+  a.parts = parts;
+  a.batch = batch;
+  a.k = k;
+  return cuda_status(launch_concat_parts(a, stream));
+}
+
+int csa2_merge_attn(int32_t parts, int32_t rows, int32_t v_dim, const float* out_parts, const float* lse_parts,
+                    float* out, float* lse, csa2_stream_t stream) {
+  if (parts < 1 || rows < 1 || v_dim < 1 || out_parts == nullptr || lse_parts == nullptr || out == nullptr)
+    return CSA2_ERR_INVALID_ARG;
+  if (parts > 1024 || v_dim > 1024 || int64_t(rows) * v_dim * parts > (int64_t(1) << 40)) return CSA2_ERR_UNSUPPORTED;
+  MergeAttnArgs a{};
+  a.out_parts = out_parts;
+  a.lse_parts = lse_parts;
+  a.out = out;
+  a.lse = lse;
+  a.parts = parts;
+  a.rows = rows;
+  a.v_dim = v_dim;
+  return cuda_status(launch_merge_attn(a, stream));
 }
 
 const char* csa2_status_str(int status) {

@@ -144,6 +144,39 @@ struct SwaAppendArgs {
   int* err;
 };
 
+// Context-parallel helpers (shard.cu).
+struct ShardSliceArgs {
+  const int* ids;            // [B, ld] ids (ascending in the uses here; -1 and ids outside [lo, hi) are dropped)
+  long long ld;
+  int lo, hi, delta;
+  int* out;                  // [B, ld_out] kept ids + delta in input order, -1 padded
+  long long ld_out;
+  int* n_out;                // [B] kept count (nullable)
+  int* err;
+};
+
+struct MergeAttnArgs {
+  const float* out_parts;    // [parts, rows, v_dim]
+  const float* lse_parts;    // [parts, rows]
+  float* out;                // [rows, v_dim]
+  float* lse;                // [rows] (nullable)
+  int parts, rows, v_dim;
+};
+
+cudaError_t launch_shard_slice(const ShardSliceArgs& a, int batch, cudaStream_t st);
+struct ConcatArgs {
+  const int* ids;            // [parts, batch, k]
+  const float* scores;       // [parts, batch, k] (nullable)
+  int* ids_out;              // [batch, parts * k]
+  float* scores_out;         // [batch, parts * k] (written when scores is not null)
+  int parts, batch, k;
+};
+
+cudaError_t launch_shard_counts(const int* n_valid, int batch, int e0, int n_loc, int div, int* out,
+                                cudaStream_t st);
+cudaError_t launch_concat_parts(const ConcatArgs& a, cudaStream_t st);
+cudaError_t launch_merge_attn(const MergeAttnArgs& a, cudaStream_t st);
+
 cudaError_t launch_kv_append(const KvAppendArgs& a, int batch, cudaStream_t st);
 cudaError_t launch_swa_append(const SwaAppendArgs& a, int batch, cudaStream_t st);
 
