@@ -22,7 +22,8 @@
 // measured to be limited by the rate at which the TMA unit accepts small
 // copies.)  Invalid slots (index -1, beyond n_swa, or unused) are zero-filled
 // by the copies themselves and masked.  Four warps each own 16 heads; their Q
-// fragments are loaded straight into registers while the gather is in flight.  S = Q K^T and O = P V run on
+// fragments are loaded straight into registers first thing, so that they are in
+// flight with the window count and the gather.  S = Q K^T and O = P V run on
 // mma.sync m16n8k16 (bf16 in, fp32 accumulate) with a base-2 fp32 softmax.
 // The partials of the cluster are merged with a single cluster barrier: every
 // CTA pushes its per-head (m, l) into the table of the CTA that owns those
@@ -108,6 +109,22 @@ __global__ void __launch_bounds__(kThreads, 2) attn_mma_kernel(const AttnArgs a)
     }
   };
 
+  // --- Q A-fragments for heads 16w + g and 16w + g + 8, straight from global; issued
+  // first, so that their latency overlaps the window count's.
+  uint32_t qa[kDk / 16][4];
+  {
+    const uint32_t* q0 = reinterpret_cast<const uint32_t*>(static_cast<const uint8_t*>(a.q) +
+                                                           ((long long)b * kH + warp * 16 + g) * (kDk * 2)) + t;
+    const uint32_t* q1 = q0 + 8 * (kDk / 2);
+#pragma unroll
+    for (int ks = 0; ks < kDk / 16; ++ks) {
+      qa[ks][0] = __ldg(q0 + ks * 8);
+      qa[ks][1] = __ldg(q1 + ks * 8);
+      qa[ks][2] = __ldg(q0 + ks * 8 + 4);
+      qa[ks][3] = __ldg(q1 + ks * 8 + 4);
+    }
+  }
+
   // --- group 0: this CTA's SWA rows (inputs of this launch), before waiting on the preceding one.
   // Local slots are handled in quads [4m, 4m + 4), quad m by warp m mod 4.
   const int ns = clamp_count(a.n_swa[b], a.swa, a.err);
@@ -122,20 +139,6 @@ __global__ void __launch_bounds__(kThreads, 2) attn_mma_kernel(const AttnArgs a)
   }
   asm volatile("cp.async.commit_group;" ::: "memory");
 
-  // --- Q A-fragments for heads 16w + g and 16w + g + 8, straight from global
-  uint32_t qa[kDk / 16][4];
-  {
-    const uint32_t* q0 = reinterpret_cast<const uint32_t*>(static_cast<const uint8_t*>(a.q) +
-                                                           ((long long)b * kH + warp * 16 + g) * (kDk * 2)) + t;
-    const uint32_t* q1 = q0 + 8 * (kDk / 2);
-#pragma unroll
-    for (int ks = 0; ks < kDk / 16; ++ks) {
-      qa[ks][0] = __ldg(q0 + ks * 8);
-      qa[ks][1] = __ldg(q1 + ks * 8);
-      qa[ks][2] = __ldg(q0 + ks * 8 + 4);
-      qa[ks][3] = __ldg(q1 + ks * 8 + 4);
-    }
-  }
   pdl_wait();   // the indices come from the preceding launch
 
   // --- main index of every slot of this warp's quads 4 * warp + 16i: lane l holds
