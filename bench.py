@@ -428,30 +428,35 @@ def run_ours(args):
     return 0
 
 
-KERNEL_SOURCES = ("fused.cu", "common.cuh", "internal.h")
+# Sources whose hash a traffic record carries, per dominant-kernel kind.
+KERNEL_SOURCES = {
+    "index_select_pooled": ("fused.cu", "common.cuh", "internal.h"),
+    "index_select_flat": ("fused.cu", "common.cuh", "internal.h"),
+    "indexer_flat": ("indexer.cu", "common.cuh", "internal.h"),
+}
 
 
-def kernel_source_hash() -> str:
-    """First 16 hex digits of the SHA-256 of the fused selection kernel's sources."""
+def kernel_source_hash(kind: str) -> str:
+    """First 16 hex digits of the SHA-256 of a dominant kernel's sources."""
     import hashlib
     h = hashlib.sha256()
-    for name in KERNEL_SOURCES:
+    for name in KERNEL_SOURCES[kind]:
         with open(os.path.join(ROOT, "sparse_attention_decode_index_gb300", "csrc", name), "rb") as f:
             h.update(f.read())
     return h.hexdigest()[:16]
 
 
-def profiled_traffic(wl, hier: bool):
+def profiled_traffic(wl, kind: str):
     """DRAM bytes per launch of the dominant kernel from the committed ncu capture
-    (profiles/<kernel>__<workload>.traffic.json, written beside its summary), or None when no
-    capture covers this workload or the kernel's source changed since it was captured."""
-    name = f"index_select_{'pooled' if hier else 'flat'}__{wl.name}.traffic.json"
+    (profiles/<kind>__<workload>.traffic.json, written beside its summary), or None when no
+    capture covers this workload or the kernel's sources changed since it was captured."""
+    name = f"{kind}__{wl.name}.traffic.json"
     path = os.path.join(ROOT, "profiles", name)
     if not os.path.exists(path):
         return None, "no ncu capture of this workload's dominant kernel"
     with open(path) as f:
         rec = json.load(f)
-    if rec.get("source_sha256_16") != kernel_source_hash():
+    if rec.get("source_sha256_16") != kernel_source_hash(kind):
         return None, "kernel source changed since the ncu capture"
     return int(rec["dram_bytes_per_launch"]), "dram__bytes_read.sum + dram__bytes_write.sum, profiles/" + name
 
@@ -510,7 +515,8 @@ def dominant_kernel_roofline(csa2, wl, d, stream, flush, args, peak, peak_src):
         alg += n_rows * 4                                 # the fp32 score of every row is written
     avg = sum(ms) / len(ms)
     gbs = alg / (avg / 1e3) / 1e9
-    traffic, traffic_src = profiled_traffic(wl, hier)
+    kind = "index_select_pooled" if hier else ("index_select_flat" if fused_flat else "indexer_flat")
+    traffic, traffic_src = profiled_traffic(wl, kind)
     return {"bound": "hbm", "kernel": name, "achieved": gbs, "peak": peak, "unit": "GB/s", "frac": gbs / peak,
             "traffic": traffic, "traffic_source": traffic_src, "alg_bytes_per_launch": alg, "launch_us": 1e3 * avg,
             "peak_source": peak_src,
