@@ -580,8 +580,11 @@ int csa2_layer_group(const csa2_shape* shape, const csa2_layer* layers, int32_t 
   const int32_t* cur = nullptr;
   for (int l = 0; l < n_layers; ++l) {
     const csa2_layer& y = layers[l];
-    // another attention-only launch next (Reuse or SWA layer): release it at this attention's end
-    const bool attn_next = l + 1 < n_layers && (layers[l + 1].mode == CSA2_REUSE || layers[l + 1].mode == CSA2_SWA);
+    // Another attention-only launch next (Reuse or SWA layer): release it at this
+    // attention's end, unless the batch is small enough that both launches' CTAs
+    // find SMs of their own (then its CTAs fetch their window rows early).
+    const bool attn_next = l + 1 < n_layers && (layers[l + 1].mode == CSA2_REUSE || layers[l + 1].mode == CSA2_SWA) &&
+                           !(attn_fast(s) && 2 * s.batch * attn_cluster(s.topk, s.swa) <= device_sm_count());
     if (y.mode == CSA2_SWA) {
       CSA2_TRY(do_attn(s, y.q, k_main, v_main, nullptr, y.k_swa, y.v_swa, n_swa, y.out, y.lse, err, stream, true,
                        attn_next));

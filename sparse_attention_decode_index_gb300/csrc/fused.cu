@@ -63,8 +63,10 @@ constexpr int kBlock = 8;
 constexpr int kBlockBytes = kBlock * kRowBytes;
 constexpr int kBlocksPerTile = kTileRows / kBlock;
 constexpr int kBins = 256;
-constexpr int kMaxCluster = 8;
+constexpr int kMaxCluster = 16;                       // 16 is a non-portable cluster size (small batches only)
+constexpr int kPortableCluster = 8;
 constexpr int kMaxRowsPerCta = 4096;                 // order keys kept in shared memory
+constexpr int kMaxRowsPerCta16 = 2048;               // with more than 8 CTAs: the cluster's keys stay < 65,536
 // After scoring, the ring buffer is reused:
 //   region A: the histogram of a cluster-wide pass, two bins per word (16-bit
 //             counters, 32 lane-private copies), then the gather buffer;
@@ -75,7 +77,7 @@ constexpr int kMaxRowsPerCta = 4096;                 // order keys kept in share
 //   region B: the per-CTA bin totals pushed by every CTA, 16-bit counts two
 //             bins per word, in two buffers.
 constexpr int kRingWords = kStages * kTileBytes / 4;
-constexpr int kLanes = 32;
+constexpr int kLanes = 16;                           // histogram copies: lanes l and l + 16 share one
 constexpr int kHistDWords = (kBins / 2) * kLanes;
 constexpr int kTotWords = kMaxCluster * kBins / 2;                  // one totals buffer
 constexpr int kRegionA = kRingWords - 2 * kTotWords;
@@ -457,7 +459,7 @@ __global__ void __launch_bounds__(kThreads, 4) index_select_kernel(const SelectA
       for (int u = 0; u < 8; ++u) {   // no branch: a key outside [lo, hi] adds 0 to a clamped bin
         const uint32_t bin = min(uint32_t(kBins - 1), bin_of(kk[u], bn));
         const uint32_t inc = (kk[u] >= lo && kk[u] <= hi) ? ((bin & 1u) ? 0x10000u : 1u) : 0u;
-        atomicAdd(&histD[(bin >> 1) * kLanes + lane], inc);
+        atomicAdd(&histD[(bin >> 1) * kLanes + (lane & (kLanes - 1))], inc);
         packed[u >> 2] |= bin << (8 * (u & 3));
       }
       kbin[i0] = packed[0];
@@ -864,10 +866,15 @@ static cudaError_t choose(bool pooled, int max_units, int batch, ClusterChoice& 
   const long long rows = (long long)max_units * unit_rows;
   long long target = (rows + kTargetRows - 1) / kTargetRows;
   target = max(target, (long long)((sms + batch - 1) / batch));
-  const int top = int(min(target, (long long)kMaxCluster));
+  // more than 8 CTAs (a non-portable cluster size) only while the whole batch's
+  // clusters of that size stay in one wave at two CTAs per SM, and only when the rows alone call for that many (about kTargetRows each)
+  const int cap = (batch * kMaxCluster <= 2 * sms && rows >= (long long)kMaxCluster * kTargetRows) ? kMaxCluster
+                                                                                                : kPortableCluster;
+  const int top = int(min(target, (long long)cap));
   ClusterChoice best;
   for (int c = max(top, 1); c >= 1; --c) {
     const int per = (max_units + c - 1) / c;
+    if (c > kPortableCluster && per * unit_rows > kMaxRowsPerCta16) continue;
     if (per * unit_rows > kMaxRowsPerCta) break;
     const size_t smem = select_smem_bytes(per, pooled);
     cudaLaunchConfig_t cfg = {};
@@ -896,7 +903,7 @@ static cudaError_t choose(bool pooled, int max_units, int batch, ClusterChoice& 
 
 bool index_select_supported(bool pooled, int max_units) {
   const int unit_rows = pooled ? kBlock : 1;
-  return (max_units + kMaxCluster - 1) / kMaxCluster * unit_rows <= kMaxRowsPerCta;
+  return (max_units + kPortableCluster - 1) / kPortableCluster * unit_rows <= kMaxRowsPerCta;
 }
 
 cudaError_t launch_index_select(const SelectArgs& in, bool pooled, int batch, int max_units, cudaStream_t st) {
@@ -906,11 +913,17 @@ cudaError_t launch_index_select(const SelectArgs& in, bool pooled, int batch, in
   // made once per (device, mode, size, batch) and kept in a small table
   // shared by all host threads.
   cudaError_t e = pooled ? once_per_device(kSetupSelectPooled, [] {
-    return cudaFuncSetAttribute(index_select_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                int(select_smem_bytes(kMaxRowsPerCta / kBlock, true)));
+    cudaError_t r = cudaFuncSetAttribute(index_select_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         int(select_smem_bytes(kMaxRowsPerCta / kBlock, true)));
+    if (r == cudaSuccess)
+      r = cudaFuncSetAttribute(index_select_kernel<true>, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+    return r;
   }) : once_per_device(kSetupSelectFlat, [] {
-    return cudaFuncSetAttribute(index_select_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                int(select_smem_bytes(kMaxRowsPerCta, false)));
+    cudaError_t r = cudaFuncSetAttribute(index_select_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         int(select_smem_bytes(kMaxRowsPerCta, false)));
+    if (r == cudaSuccess)
+      r = cudaFuncSetAttribute(index_select_kernel<false>, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+    return r;
   });
   if (e != cudaSuccess) return e;
   struct Entry {
