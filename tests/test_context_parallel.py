@@ -25,18 +25,19 @@ def _free_port():
         return s.getsockname()[1]
 
 
-def _workload():
+def _workload(hier_full=0):
     sh = W.Shape(batch=3, n_entries=2048, pool_blocks=32, topk=64, q_heads=8, k_dim=32, v_dim=16, swa=16)
     modes = [W.FULL, W.REUSE, W.REINDEX, W.REUSE, W.SWA]
-    return W.make_workload(sh, modes, seed=5, cfg_id=80, n_valid=[2048, 1500, 37], n_swa=[16, 9, 0])
+    return W.make_workload(sh, modes, seed=5, cfg_id=80, n_valid=[2048, 1500, 37], n_swa=[16, 9, 0],
+                           hier_full=hier_full)
 
 
-def _rank_main(rank, world, port, out):
+def _rank_main(rank, world, port, out, hier_full=0):
     os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port))
     dist.init_process_group("gloo", rank=rank, world_size=world)
     try:
         from tests.cp_helpers import OracleOps
-        wl = _workload()
+        wl = _workload(hier_full)
         sh = wl.shape
         plan = CP.ShardPlan(sh.n_entries, world, sh.block)
         f = lambda a: torch.from_numpy(np.ascontiguousarray(oracle.to_f64(a)))   # noqa: E731
@@ -68,12 +69,14 @@ def _rank_main(rank, world, port, out):
         dist.destroy_process_group()
 
 
-@pytest.mark.parametrize("world", [2, 4])
-def test_context_parallel_group_equals_the_unsharded_oracle_with_gloo(world):
+@pytest.mark.parametrize("world,hier_full", [(2, 0), (4, 0), (3, 1)])
+def test_context_parallel_group_equals_the_unsharded_oracle_with_gloo(world, hier_full):
+    """World sizes 2 and 4 split the 256 blocks evenly; 3 splits them 86 / 86 / 84 and also
+    runs the Full layer hierarchically (its pool of 32 blocks then comes from three ranks)."""
     port = _free_port()
     ctx = mp.get_context("spawn")
     out = ctx.Manager().dict()
-    procs = [ctx.Process(target=_rank_main, args=(r, world, port, out)) for r in range(world)]
+    procs = [ctx.Process(target=_rank_main, args=(r, world, port, out, hier_full)) for r in range(world)]
     for p in procs:
         p.start()
     for p in procs:
