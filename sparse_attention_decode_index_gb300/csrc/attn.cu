@@ -25,16 +25,16 @@
 // fragments are loaded straight into registers first thing, so that they are in
 // flight with the window count and the gather.  S = Q K^T and O = P V run on
 // mma.sync m16n8k16 (bf16 in, fp32 accumulate) with a base-2 fp32 softmax.
-// The partials of the cluster are merged with a single cluster barrier: every
-// CTA pushes its per-head (m, l) into the table of the CTA that owns those
-// heads (distributed shared memory) and writes its unscaled partial O, as
-// 16-byte vectors assembled from lane pairs, to workspace scratch that stays
-// in L2; the owner then weights the partials by exp2(m_c - M) / L, sums them
-// in fixed CTA order, so the result is deterministic, and drops their L2 lines
-// (discard, no write-back: every launch rewrites them).  (Pushing the partials
-// through distributed shared memory instead needs a second barrier -- they
-// would land in the K region while a peer may still be reading it -- and was
-// measured slower.)
+// The partials of the cluster are merged through distributed shared memory:
+// every CTA pushes its per-head (m, l) into the table of the CTA that owns
+// those heads and leaves its unscaled partial O of all heads in its own K
+// region (free once its warps are done with the keys and values).  After one
+// cluster barrier the owner weights the partials by exp2(m_c - M) / L and sums
+// them in fixed CTA order, so the result is deterministic, reading its peers'
+// partials with distributed shared-memory loads; a second, split barrier keeps
+// every CTA resident until its partials have been read.  (Writing the partials
+// to workspace scratch in L2 instead was measured slower at small batches and
+// equal at batch 64.)
 #include "common.cuh"
 #include "internal.h"
 

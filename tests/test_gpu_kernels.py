@@ -248,6 +248,32 @@ def test_sparse_attn(csa2, fast):
     assert_no_device_error(csa2, ws)
 
 
+@pytest.mark.parametrize("K,Wn", [(128, 16), (256, 32), (384, 64), (700, 64), (800, 64), (896, 128)])
+def test_sparse_attn_cluster_sizes(csa2, K, Wn):
+    """Clusters of 1, 2, 3, 5, 6 and 7 CTAs (the smallest C with ceil(K / C) + ceil(Wn / C) <= 160
+    slots; K + Wn <= 1024 keeps C below 8): every CTA merges ceil(64 / C) heads, the last fewer
+    when C does not divide 64."""
+    rng = np.random.default_rng(K + Wn)
+    B, N, H, dk, dv = 5, 3000, 64, 192, 128
+    sh = _shape(batch=B, n_entries=N, q_heads=H, k_dim=dk, v_dim=dv, topk=K, swa=Wn, pool_blocks=0)
+    assert csa2.fast_path(sh)[1]
+    q, km, vm, ks, vs, idx = _attn_case(rng, B, N, H, dk, dv, K, Wn)
+    n_swa = np.array([Wn, 3, 0, 0, 1], dtype=np.int32)   # row 3: no key at all (lse -inf, output 0)
+    out = torch.full((B, H, dv), 3.0, dtype=torch.float32, device="cuda")
+    lse = torch.zeros((B, H), dtype=torch.float32, device="cuda")
+    ws = csa2.workspace(sh)
+    csa2.sparse_attn(sh, bf16(q), bf16(km), bf16(vm), i32(idx), bf16(ks), bf16(vs), i32(n_swa), out, ws, lse=lse)
+    o, l = out.cpu().numpy(), lse.cpu().numpy()
+    ref_o, ref_l = np.zeros((B, H, dv)), np.zeros((B, H))
+    for b in range(B):
+        ref_o[b], ref_l[b] = oracle.sparse_attention(oracle.to_f64(q[b]), oracle.to_f64(km[b]),
+                                                     oracle.to_f64(vm[b]), idx[b].astype(np.int64),
+                                                     oracle.to_f64(ks[b]), oracle.to_f64(vs[b]), int(n_swa[b]),
+                                                     1 / math.sqrt(dk))
+    compare_attention(o, l, ref_o, ref_l, atol=1e-2)
+    assert_no_device_error(csa2, ws)
+
+
 def test_sparse_attn_flags_out_of_range_index(csa2):
     rng = np.random.default_rng(6)
     B, N = 2, 1000
