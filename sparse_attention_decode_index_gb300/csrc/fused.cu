@@ -225,6 +225,7 @@ __global__ void __launch_bounds__(kThreads, 4) index_select_kernel(const SelectA
   const int ntiles = (rows_total + kTileRows - 1) / kTileRows;
   const uint8_t* keys = static_cast<const uint8_t*>(a.keys) + (long long)(b / a.seq_div) * a.rows_per_seq * kRowBytes;
   if (warp == kConsumers) {
+    const uint64_t pol = l2_evict_first();   // every key row is read once
     int i = 0;
     for (; i < ntiles; ++i) {
       const int s = i % kStages;
@@ -238,7 +239,7 @@ __global__ void __launch_bounds__(kThreads, 4) index_select_kernel(const SelectA
           const int r0 = begin + i * kTileRows;
           const uint32_t bytes = uint32_t(min(kTileRows, end - r0)) * kRowBytes;
           mbar_arrive_expect_tx(&sm.full[s], bytes);
-          if (copy) bulk_g2s(dst, keys + (long long)r0 * kRowBytes, bytes, &sm.full[s]);
+          if (copy) bulk_g2s_hint(dst, keys + (long long)r0 * kRowBytes, bytes, &sm.full[s], pol);
         }
       } else {
         const int p0 = i * kBlocksPerTile;
@@ -248,7 +249,7 @@ __global__ void __launch_bounds__(kThreads, 4) index_select_kernel(const SelectA
         if (lane == 0) mbar_arrive_expect_tx(&sm.full[s], uint32_t(__popc(have)) * kBlockBytes);
         __syncwarp();
         if (blk >= 0 && copy)
-          bulk_g2s(dst + lane * kBlockBytes, keys + (long long)blk * kBlockBytes, kBlockBytes, &sm.full[s]);
+          bulk_g2s_hint(dst + lane * kBlockBytes, keys + (long long)blk * kBlockBytes, kBlockBytes, &sm.full[s], pol);
       }
     }
     if (lane == 0) {

@@ -101,6 +101,7 @@ __global__ void __launch_bounds__(kThreads) indexer_mma_kernel(const IndexerArgs
 
   if (warp == kConsumers) {
     // ---------------- producer warp
+    const uint64_t pol = l2_evict_first();   // every key row is read once
     int i = 0;
     for (; i < ntiles; ++i) {
       const int s = i % kStages;
@@ -113,7 +114,7 @@ __global__ void __launch_bounds__(kThreads) indexer_mma_kernel(const IndexerArgs
           const int r0 = begin + i * kTileRows;
           const uint32_t bytes = uint32_t(min(kTileRows, end - r0)) * kRowBytes;
           mbar_arrive_expect_tx(&full[s], bytes);
-          bulk_g2s(dst, keys + (long long)r0 * kRowBytes, bytes, &full[s]);
+          bulk_g2s_hint(dst, keys + (long long)r0 * kRowBytes, bytes, &full[s], pol);
         }
       } else {
         const int p0 = i * kBlocksPerTile;
@@ -123,7 +124,7 @@ __global__ void __launch_bounds__(kThreads) indexer_mma_kernel(const IndexerArgs
         if (lane == 0) mbar_arrive_expect_tx(&full[s], uint32_t(__popc(have)) * kBlockBytes);
         __syncwarp();
         if (blk >= 0)
-          bulk_g2s(dst + lane * kBlockBytes, keys + (long long)blk * kBlockBytes, kBlockBytes, &full[s]);
+          bulk_g2s_hint(dst + lane * kBlockBytes, keys + (long long)blk * kBlockBytes, kBlockBytes, &full[s], pol);
       }
     }
     if (lane == 0) {
