@@ -259,6 +259,9 @@ def test_sparse_attn_cluster_sizes(csa2, K, Wn):
     assert csa2.fast_path(sh)[1]
     q, km, vm, ks, vs, idx = _attn_case(rng, B, N, H, dk, dv, K, Wn)
     n_swa = np.array([Wn, 3, 0, 0, 1], dtype=np.int32)   # row 3: no key at all (lse -inf, output 0)
+    for b in range(B):   # window rows past the count are not part of the window: NaN must not leak
+        ks[b, n_swa[b]:] = 0x7fc0
+        vs[b, n_swa[b]:] = 0x7fc0
     out = torch.full((B, H, dv), 3.0, dtype=torch.float32, device="cuda")
     lse = torch.zeros((B, H), dtype=torch.float32, device="cuda")
     ws = csa2.workspace(sh)
