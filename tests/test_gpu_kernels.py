@@ -338,6 +338,40 @@ def test_index_topk_fused(csa2, mode):
     assert_no_device_error(csa2, ws)
 
 
+@pytest.mark.parametrize("mode", ["flat", "pooled"])
+def test_index_topk_fused_clusters_of_16(csa2, mode):
+    """Small batches over many rows take clusters of 16 CTAs (a non-portable size): 32,768
+    flat rows (2,048 per CTA), or a pool of 2,048 blocks (16,384 rows, 1,024 per CTA).
+    Integer keys tie heavily; one query is ragged, one nearly empty."""
+    rng = np.random.default_rng(16)
+    B, N, P = 3, 32768, 2048
+    sh = _shape(batch=B, n_entries=N, pool_blocks=P if mode == "pooled" else 0, topk=512)
+    k_idx = _int_keys(rng, (B, N, sh.idx_dim))
+    q_idx = _int_keys(rng, (B, sh.idx_heads, sh.idx_dim))
+    w = rng.integers(1, 4, size=(B, sh.idx_heads)).astype(np.float32)
+    n_valid = np.array([N, 20001, 777], dtype=np.int32)
+    ws = csa2.workspace(sh)
+    pool = n_pool = None
+    if mode == "pooled":
+        kb = torch.zeros((B, N // 8, sh.idx_dim), dtype=torch.bfloat16, device="cuda")
+        csa2.block_keys(sh, bf16(k_idx), i32(n_valid), kb, ws, round_to_int=True)
+        pool = torch.zeros((B, P), dtype=torch.int32, device="cuda")
+        n_pool = torch.zeros(B, dtype=torch.int32, device="cuda")
+        csa2.index_blocks(sh, bf16(q_idx), f32(w), kb, i32(n_valid), pool, n_pool, ws)
+    for k in (512, 37):
+        idx = torch.full((B, k), -9, dtype=torch.int32, device="cuda")
+        csa2.index_topk(sh, bf16(q_idx), f32(w), bf16(k_idx), i32(n_valid), k, idx, ws, pool=pool, n_pool=n_pool)
+        got = idx.cpu().numpy()
+        for b in range(B):
+            keys = oracle.to_f64(k_idx[b])
+            n = int(n_valid[b])
+            kb_o = oracle.block_keys(keys, n, 8, True) if mode == "pooled" else None
+            r = oracle.layer_indices(oracle.to_f64(q_idx[b]), w[b].astype(np.float64), keys, kb_o, n, topk=k,
+                                     block=8, pool=P, hier=mode == "pooled")
+            assert got[b].tolist() == r["idx"].tolist(), f"{mode} k={k} query {b}"
+    assert_no_device_error(csa2, ws)
+
+
 @pytest.mark.parametrize("group,spread", [(1000, 2), (1000, 1), (340, 1), (280, 1), (280, 2)])
 def test_index_topk_fused_large_threshold_bin(csa2, group, spread):
     """Fused flat scoring + Top-k when the bin holding the k-th score gathers `group`
