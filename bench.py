@@ -437,12 +437,19 @@ KERNEL_SOURCES = {
 
 
 def kernel_source_hash(kind: str) -> str:
-    """First 16 hex digits of the SHA-256 of a dominant kernel's sources."""
+    """First 16 hex digits of the SHA-256 of a dominant kernel's sources, with
+    comments and blank lines left out (an edit of the documentation alone does not
+    make a traffic capture stale)."""
     import hashlib
+    import re
     h = hashlib.sha256()
     for name in KERNEL_SOURCES[kind]:
-        with open(os.path.join(ROOT, "sparse_attention_decode_index_gb300", "csrc", name), "rb") as f:
-            h.update(f.read())
+        with open(os.path.join(ROOT, "sparse_attention_decode_index_gb300", "csrc", name)) as f:
+            text = re.sub(r"/\*.*?\*/", "", f.read(), flags=re.S)
+        for line in text.splitlines():
+            code = re.sub(r"//.*$", "", line).rstrip()
+            if code:
+                h.update(code.encode() + b"\n")
     return h.hexdigest()[:16]
 
 

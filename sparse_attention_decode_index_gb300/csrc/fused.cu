@@ -69,7 +69,7 @@ constexpr int kMaxRowsPerCta = 4096;                 // order keys kept in share
 constexpr int kMaxRowsPerCta16 = 2048;               // with more than 8 CTAs: the cluster's keys stay < 65,536
 // After scoring, the ring buffer is reused:
 //   region A: the histogram of a cluster-wide pass, two bins per word (16-bit
-//             counters, 32 lane-private copies), then the gather buffer;
+//             counters, 16 copies shared by lanes l and l + 16), then the gather buffer;
 //             its tail first holds the bin of every key of the last pass (one
 //             byte per key, so that later tests need no binning), then the
 //             histogram (kCopiesL copies) and totals of the passes over the
