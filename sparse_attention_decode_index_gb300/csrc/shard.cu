@@ -38,7 +38,7 @@ __global__ void __launch_bounds__(kSliceThreads) shard_slice_kernel(const ShardS
   for (int p0 = 0; p0 < a.ld; p0 += kSliceThreads) {
     const int p = p0 + tid;
     const int id = p < a.ld ? in[p] : -1;
-    const bool keep = id >= a.lo && id < a.hi;
+    const bool keep = id >= 0 && id >= a.lo && id < a.hi;   // -1 pads are never kept
     const unsigned m = __ballot_sync(0xffffffffu, keep);
     if (lane == 0) warp_tot[warp] = __popc(m);
     __syncthreads();
