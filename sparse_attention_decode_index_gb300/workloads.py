@@ -28,6 +28,9 @@ plus a 128-token SWA window, blocks of 8, a pool of at most 2,048 blocks):
   2,048 blocks.
 * ``dec_b16_1m`` -- decoder group Full + 3 Reuse + [Reindex + 3 Reuse] x 4,
   batch 16, 1,048,576 tokens at ratio 4 (262,144 entries).
+* ``dec_b16_1m_hier`` -- ``dec_b16_1m`` with its Full layer hierarchical too
+  (block scoring over 32,768 blocks and a pool of 2,048 instead of the flat
+  scan of 262,144 entries).
 * ``enc_stack_b32_32k`` -- the whole 20-layer encoder stack SWA, SWA,
   [Full + 5 Reuse] x 3 at the shapes of ``enc_b32_32k`` (pure SWA layers attend
   their window only).
@@ -304,6 +307,10 @@ WORKLOADS = {
                               context=32768),
     "dec_b16_1m": dict(cfg_id=4, batch=16, n_entries=262144, modes=decoder_group_modes(),
                        pool=2048, context=1048576),
+    # the 1M decoder group with its Full layer hierarchical too (block scoring and a
+    # 2,048-block pool instead of the 262,144-entry flat scan)
+    "dec_b16_1m_hier": dict(cfg_id=4, batch=16, n_entries=262144, modes=decoder_group_modes(),
+                            pool=2048, context=1048576, hier_full=1),
     # the 20-layer decoder group at the 128K Reindex workload's context and batch
     "dec_b64_128k": dict(cfg_id=7, batch=64, n_entries=32768, modes=decoder_group_modes(), pool=2048,
                          context=131072),
@@ -323,6 +330,7 @@ def named(name: str, seed: int = 0, batch: Optional[int] = None) -> Workload:
                               pool=spec["pool"], modes=spec["modes"], seed=seed, cfg_id=spec["cfg_id"], name=name)
     shape = Shape(batch=batch or spec["batch"], n_entries=spec["n_entries"],
                   pool_blocks=spec["pool"])
-    wl = make_workload(shape, spec["modes"], seed=seed, cfg_id=spec["cfg_id"], name=name)
+    wl = make_workload(shape, spec["modes"], seed=seed, cfg_id=spec["cfg_id"], name=name,
+                       hier_full=spec.get("hier_full", 0))
     wl.note = f"{spec['context']} tokens at ratio 4"
     return wl

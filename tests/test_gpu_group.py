@@ -52,7 +52,7 @@ def check_group(csa2, wl, d, queries=None, atol=1e-2):
 
 
 @pytest.mark.parametrize("name", ["full_b8_8k", "enc_b32_32k", "reindex_b64_128k", "dec_b16_1m",
-                                  "enc_stack_b32_32k", "dec_b64_128k"])
+                                  "dec_b16_1m_hier", "enc_stack_b32_32k", "dec_b64_128k"])
 def test_named_workload(csa2, name):
     """Every query of the named workload at full size, in the launch configuration the bench
     times (one csa2_layer_group call), against the oracle: indices bit-exact, outputs within 1e-2."""
