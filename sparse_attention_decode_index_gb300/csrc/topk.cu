@@ -96,8 +96,11 @@ __device__ __forceinline__ void block_minmax(uint32_t& lo, uint32_t& hi, uint32_
   __syncthreads();
 }
 
+// Two CTAs per SM (64 registers, a few hundred bytes of spills at IPT = 32):
+// the 1M decoder group's 256 chunk CTAs then run in one wave instead of 1.7
+// (measured 565.3 -> 562.9 us per group step).
 template <int IPT>
-__global__ void __launch_bounds__(kThreads) topk_kernel(const TopkArgs a) {
+__global__ void __launch_bounds__(kThreads, 2) topk_kernel(const TopkArgs a) {
   __shared__ TopkSmem sm;
   const int b = blockIdx.y, c = blockIdx.x, tid = threadIdx.x;
   pdl_launch_dependents();
